@@ -1,0 +1,408 @@
+"""Benchmark of the paged fused-MoE layer (one GB300, or N independent replicas).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole layer (route, align, gather, GEMM 1 + SwiGLU, GEMM 2,
+combine) over one batch of synthetic tokens, through the C ABI on device-resident inputs.
+The default workload is the Qwen3-30B-A3B-shaped layer with 64 decode tokens; its expert
+pages (about 1.2 GB touched per step) exceed the 129 MB L2, so no flush is needed between
+steps.  Rank 0 prints one JSON line.  ``--impl reference`` times the CPU oracle on the
+host cores instead (a deliberately slow baseline, not a target).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged fused-MoE tokens/s; % of HBM / bf16 tensor roofline (Qwen3-30B-A3B)"
+DEFAULT_STEPS = {"q3_decode": 2000, "q3_prefill_zipf": 100, "q35_mixed_pool": 500, "tiny": 2000}
+WORKLOAD_TEXT = {
+    "q3_decode": "Qwen3-30B-A3B-shaped MoE layer, decode: hidden 2048, moe intermediate 768, "
+                 "128 experts, top-8 renormalised, 64 tokens; each w1/w3/w2 one 3 MiB page "
+                 "shuffled across a 1024-page pool, unused pages NaN",
+    "q3_prefill_zipf": "same Qwen3-30B-A3B-shaped layer, prefill: 8192 tokens, router logits "
+                       "= x.Wg + per-expert Zipf(s=1.1) bias",
+    "q35_mixed_pool": "Qwen3.5-35B-A3B-shaped MoE layer: hidden 2048, intermediate 512, 256 "
+                      "experts, top-8; 2 MiB expert pages interleaved with huge pages split "
+                      "into 32 KiB KV blocks",
+    "tiny": "tiny paged MoE layer: hidden 256, intermediate 128, 8 experts, top-2, 16 tokens",
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"rimuru_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        mhz, maxmhz, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    mhz.append(float(parts[1]))
+                    maxmhz = max(maxmhz, float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.remove(self.path)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": maxmhz,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def source_digest(*rel_paths):
+    h = hashlib.sha256()
+    for p in rel_paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ("paged_moe_shared_gb300/csrc/moe_gemm.cu", "paged_moe_shared_gb300/csrc/device.cuh")
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    rec = t.get(workload, {}).get(kernel)
+    if not rec or rec.get("source_digest") != source_digest(*GEMM_SOURCES):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def kernel_work(w, counts):
+    """Algorithmic bytes and flops per launch of each kernel (no padding, no re-reads)."""
+    s = w.shape
+    T, H, I, E, k = w.T, s.H, s.I, s.E, s.k
+    A = T * k
+    U = int((counts > 0).sum())
+    return {
+        "moe_route": {"bytes": T * E * 4 + A * 8, "flops": 0},
+        "moe_align": {"bytes": A * 4 * 3, "flops": 0},
+        "moe_gather": {"bytes": 2 * A * H * 2, "flops": 0},
+        "moe_gemm1_swiglu": {"bytes": U * 2 * H * I * 2 + A * H * 2 + A * I * 2,
+                             "flops": 2 * A * H * 2 * I},
+        "moe_gemm2": {"bytes": U * I * H * 2 + A * I * 2 + A * H * 2, "flops": 2 * A * I * H},
+        "moe_combine": {"bytes": A * H * 2 + T * H * 2 + A * 8, "flops": 2 * A * H},
+        "layer": {"bytes": U * 3 * H * I * 2 + T * H * 2 + T * E * 4 + T * H * 2,
+                  "flops": 6 * A * H * I},
+        "U": U,
+    }
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import workloads as wl
+    from paged_moe_shared_gb300 import rimuru as R
+    from paged_moe_shared_gb300.device_pool import load_workload
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    w = wl.CONFIGS[args.workload](seed=args.seed) if args.tokens is None else \
+        wl.CONFIGS[args.workload](seed=args.seed, T=args.tokens)
+    pool, ev, _ = load_workload(w, dev)
+    x = torch.from_numpy(w.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    logits = torch.from_numpy(w.logits).to(dev)
+    out = torch.empty_like(x)
+    ws_bytes = R.rimuru_moe_workspace_bytes(ev, w.T)
+    ws_raw = torch.empty(ws_bytes + 1024, dtype=torch.uint8, device=dev)
+    ws_ptr = (ws_raw.data_ptr() + 1023) // 1024 * 1024
+    stream = torch.cuda.current_stream()
+
+    def step():
+        R.rimuru_moe_forward(x.data_ptr(), logits.data_ptr(), w.T, ev, 0, out.data_ptr(), ws_ptr,
+                             ws_bytes, stream.cuda_stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if R.rimuru_get_device_error(ev) != R.DEV_OK:
+        raise RuntimeError("device error during warm-up")
+    lay = R.rimuru_moe_workspace_layout(ev, w.T)
+    at = ws_ptr - ws_raw.data_ptr() + lay["offsets"]
+    offs = ws_raw[at:at + (w.shape.E + 1) * 4].view(torch.int32).cpu().numpy()
+    counts = np.diff(offs)
+    work = kernel_work(w, counts)
+
+    # ---------------------------------------------------------------- timed region
+    K = args.steps
+    R.rimuru_profile_enable(ev, True, K)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    R.rimuru_profile_enable(ev, False, 1)
+    per_kernel = {}
+    for kidx in range(R.K_COUNT):
+        n, ms = R.rimuru_profile_read(ev, kidx)
+        per_kernel[R.rimuru_kernel_name(kidx)] = {"launches": n, "ms_per_launch": ms / max(n, 1)}
+    if R.rimuru_get_device_error(ev) != R.DEV_OK:
+        raise RuntimeError("device error in the timed region")
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / K
+    value = world * w.T * K / (ms_total / 1e3)
+
+    # ---------------------------------------------------------------- end to end
+    Ke = min(K, args.e2e_steps)
+    hx = torch.from_numpy(w.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hl = torch.from_numpy(w.logits).pin_memory()
+    ho = torch.empty_like(hx).pin_memory()
+    for _ in range(3):
+        x.copy_(hx, non_blocking=True)
+        logits.copy_(hl, non_blocking=True)
+        step()
+        ho.copy_(out, non_blocking=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        x.copy_(hx, non_blocking=True)
+        logits.copy_(hl, non_blocking=True)
+        step()
+        ho.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e_value = world * w.T * Ke / (ms_e2e / 1e3)
+
+    # ---------------------------------------------------------------- roofline
+    peaks = load_peaks()
+    decode_like = work["layer"]["flops"] / work["layer"]["bytes"] < 0.5 * (
+        peaks["bf16_tflops_sustained"] * 1e12) / (peaks["hbm_gbs"] * 1e9)
+    dom = max(("moe_gemm1_swiglu", "moe_gemm2"), key=lambda n: per_kernel[n]["ms_per_launch"])
+    t_dom = per_kernel[dom]["ms_per_launch"] / 1e3
+    if decode_like:
+        achieved = work[dom]["bytes"] / t_dom / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = work[dom]["flops"] / t_dom / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops_sustained"], 4)}
+    roof["kernel"] = dom
+    roof["traffic"] = ncu_traffic(dom, args.workload)
+    roof["peak_source"] = peaks["source"] + (" (sustained bf16)" if not decode_like else " (HBM copy)")
+    total_k = sum(v["ms_per_launch"] for v in per_kernel.values())
+    for name, v in per_kernel.items():
+        v["share"] = round(v["ms_per_launch"] / total_k, 4) if total_k else None
+        tk = v["ms_per_launch"] / 1e3
+        if tk > 0:
+            v["GB/s"] = round(work[name]["bytes"] / tk / 1e9, 1)
+            if work[name]["flops"]:
+                v["TFLOP/s"] = round(work[name]["flops"] / tk / 1e12, 1)
+        v["ms_per_launch"] = round(v["ms_per_launch"], 5)
+    layer_t = ms_step / 1e3
+    layer_roof = {"hbm_frac": round(work["layer"]["bytes"] / layer_t / 1e9 / peaks["hbm_gbs"], 4),
+                  "tensor_frac": round(work["layer"]["flops"] / layer_t / 1e12
+                                       / peaks["bf16_tflops_sustained"], 4)}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}", "tokens": w.T,
+                   "experts_touched": work["U"], "seed": args.seed,
+                   "l2": "inputs larger than L2: the expert pages read per step exceed 129 MB"
+                   if work["layer"]["bytes"] > 129e6 else "inputs fit in L2 (no flush)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "layer_roofline": layer_roof,
+        "kernels": per_kernel,
+        "gpu_launches": R.K_COUNT * K,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x.numel() * 2 + logits.numel() * 4),
+                "d2h_bytes_per_step": int(out.numel() * 2), "steps": Ke,
+                "ms_per_step": round(ms_e2e / Ke, 5)},
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    pool.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return result
+
+
+def oracle_sample(w, tokens):
+    import oracle
+    o = oracle.Oracle()
+    s = w.shape
+    t0 = time.perf_counter()
+    o.moe_forward(w.x_bits, w.logits, w.pool, w.page_bytes, w.page_table, s.H, s.I, s.k,
+                  s.renorm, tokens=tokens)
+    return time.perf_counter() - t0, o.max_threads()
+
+
+def sample_tokens(w, budget_s):
+    """Tokens per oracle step: enough to take roughly budget_s on the host cores, at most T."""
+    n = min(w.T, 8)
+    dt, cores = oracle_sample(w, np.arange(n))
+    while n < w.T and dt < budget_s / 4:
+        n = min(w.T, n * 4)
+        dt, cores = oracle_sample(w, np.arange(n))
+    return n, dt, cores
+
+
+def cpu_baseline(w, budget_s):
+    n, dt, cores = sample_tokens(w, budget_s)
+    reps, total = 1, dt
+    while total < budget_s * 0.5 and reps < 8:
+        d, _ = oracle_sample(w, np.arange(n))
+        total += d
+        reps += 1
+    return {"value": round(n * reps / total, 3), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n} of {w.T} tokens (all routing for {w.T}), {reps} pass(es), "
+                      f"{total:.1f} s of CPU time"}
+
+
+def run_reference(args):
+    import workloads as wl
+    w = wl.CONFIGS[args.workload](seed=args.seed) if args.tokens is None else \
+        wl.CONFIGS[args.workload](seed=args.seed, T=args.tokens)
+    n, dt, cores = sample_tokens(w, budget_s=max(2.0, 120.0 / max(args.steps + args.warmup, 1)))
+    toks = np.arange(n)
+    for _ in range(args.warmup):
+        oracle_sample(w, toks)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(w, toks)
+    total = time.perf_counter() - t0
+    value = n * args.steps / total
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}", "tokens": w.T,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{n} of {w.T} tokens per step (routing for all {w.T})"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="q3_decode", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--tokens", type=int, default=None)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.workload]
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if world != args.gpus:
+        world = max(world, 1)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,310 @@
+/*
+ * rimuru.h - C ABI of the GB300 paged fused-MoE library (librimuru.so).
+ *
+ * The library implements one hot path of Rimuru ("Rimuru: Unified Memory
+ * Management for Modern LLM Serving via Elastic Expert Offloading", arXiv
+ * 2610.40305): a fused MoE layer whose expert projection matrices are read in
+ * place from non-contiguous pages of one shared device pool, through an expert
+ * memory view (a page size plus a page table), with no gather into a
+ * contiguous buffer.  Around it sits the host-side page allocator that places
+ * pages of several views in that pool (huge pages split into expert-sized
+ * pages, expert-sized pages split into KV-sized pages, and merged back).
+ *
+ * Conventions for every function below:
+ *  - Return value: RIMURU_OK (0) or a negative rimuru_status.  No function
+ *    aborts the process; on failure a message is available from
+ *    rimuru_last_error() on the calling thread.
+ *  - Ownership: the caller owns all device memory it passes in (the pool, x,
+ *    logits, out, workspace).  The library owns its host metadata and, per
+ *    expert view with an MoE shape, one small device buffer (page table plus a
+ *    device error word) allocated on first use and freed by
+ *    rimuru_view_destroy().
+ *  - Pointers named dev_* or documented as device pointers must be device
+ *    memory of the current CUDA device; host pointers are plain host memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Forward calls are asynchronous on that stream.
+ *  - Handles are not safe to use concurrently from several threads unless
+ *    stated; the pool serialises its own allocator calls with a lock.
+ */
+#ifndef RIMURU_H_
+#define RIMURU_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct rimuru_pool_s* rimuru_pool_t;
+typedef struct rimuru_view_s* rimuru_view_t;
+
+typedef enum rimuru_status {
+  RIMURU_OK = 0,
+  RIMURU_ERR_ARG = -1,         /* null handle/pointer, negative or zero size, bad index */
+  RIMURU_ERR_ALIGN = -2,       /* pointer or size does not meet the stated alignment */
+  RIMURU_ERR_OOM = -3,         /* no free page at any level that could be split */
+  RIMURU_ERR_UNMAPPED = -4,    /* a projection of the requested layer has no page */
+  RIMURU_ERR_RANGE = -5,       /* page id, layer, expert or projection out of range */
+  RIMURU_ERR_WORKSPACE = -6,   /* workspace smaller than rimuru_moe_workspace_bytes() */
+  RIMURU_ERR_CUDA = -7,        /* a CUDA runtime or driver call failed */
+  RIMURU_ERR_DEVICE = -8,      /* a kernel reported an error through the device error word */
+  RIMURU_ERR_STATE = -9,       /* call not valid in the current state (see each function) */
+  RIMURU_ERR_UNSUPPORTED = -10 /* shape outside what the kernels handle */
+} rimuru_status;
+
+/* Projection index inside one expert (Table 1 of the Rimuru page lists the
+ * three projection matrices of an expert: w1 and w3 [hidden, inter], w2
+ * [inter, hidden]). */
+enum { RIMURU_PROJ_W1 = 0, RIMURU_PROJ_W3 = 1, RIMURU_PROJ_W2 = 2 };
+
+/* Device error codes written by kernels (read with rimuru_get_device_error). */
+enum {
+  RIMURU_DEV_OK = 0,
+  RIMURU_DEV_BAD_PAGE = 1,      /* a page-table entry outside the view: tile skipped */
+  RIMURU_DEV_NONFINITE = 2,     /* a router logit was NaN or infinite */
+  RIMURU_DEV_TIMEOUT = 3,       /* a bounded wait inside a kernel gave up */
+  RIMURU_DEV_BAD_SHAPE = 4      /* device-side tables disagree with the launch shape */
+};
+
+/* ------------------------------------------------------------------ errors */
+
+/* Message for the last failing call on this thread ("" if none).  The
+ * string stays valid until the next library call on the same thread. */
+const char* rimuru_last_error(void);
+
+/* Name of a rimuru_status value ("RIMURU_ERR_ARG", ...). */
+const char* rimuru_status_string(int status);
+
+/* ------------------------------------------------------------------- pool */
+
+/*
+ * Shared page pool (Rimuru page, abstract: "a shared page pool" over which
+ * heterogeneous tensors share device memory; explainer page: the pool is cut
+ * into huge pages).
+ *
+ * dev_base          device pointer to `bytes` bytes owned by the caller; must
+ *                   be 2 MiB aligned (over-allocate and align up).
+ * bytes             pool size; a positive multiple of huge_page_bytes.
+ * huge_page_bytes   size of the top-level pages; a positive multiple of 256.
+ *                   Use rimuru_huge_page_bytes() for the paper's rule.
+ * out               receives the handle.
+ * Errors: RIMURU_ERR_ARG (null, zero sizes), RIMURU_ERR_ALIGN (alignment or
+ * bytes not a multiple of huge_page_bytes).
+ * The pool never touches device memory: it only places pages.
+ */
+int rimuru_pool_create(void* dev_base, uint64_t bytes, uint64_t huge_page_bytes,
+                       rimuru_pool_t* out);
+
+/* Destroy a pool.  RIMURU_ERR_STATE while views of it still exist. */
+int rimuru_pool_destroy(rimuru_pool_t pool);
+
+/*
+ * Huge-page size rule (explainer page, memory-manager paragraph: the pool is
+ * cut into huge pages whose size is the least common multiple of the expert
+ * page size and the state-space-model page size, so that no page of one type
+ * straddles a huge-page boundary).  ssm_page_bytes == 0 means the model has
+ * no SSM state and the result is expert_page_bytes.  Returns 0 on a zero
+ * expert size or on overflow.
+ */
+uint64_t rimuru_huge_page_bytes(uint64_t expert_page_bytes, uint64_t ssm_page_bytes);
+
+/* Allocator occupancy, for one level (page size) of the pool. */
+typedef struct rimuru_level_stats {
+  uint64_t page_bytes;   /* page size of this level */
+  int64_t pages_total;   /* pool_bytes / page_bytes */
+  int64_t pages_free;    /* pages of this level on its free list */
+  int64_t pages_owned;   /* pages handed to views */
+  int64_t pages_split;   /* pages cut into pages of the next level */
+} rimuru_level_stats;
+
+/* Number of levels (distinct page sizes: the huge page plus every view size). */
+int rimuru_pool_num_levels(rimuru_pool_t pool, int* levels);
+/* Stats of level `level` (0 = huge pages, larger = smaller pages). */
+int rimuru_pool_level_stats(rimuru_pool_t pool, int level, rimuru_level_stats* out);
+
+/* ------------------------------------------------------------------ views */
+
+/*
+ * Memory view (Rimuru page, abstract and Figure 6 "multi-view memory
+ * layout": each tensor type interprets the shared space with its own page
+ * size and its own page table).  Page `i` of a view is the byte range
+ * [i * page_bytes, (i + 1) * page_bytes) of the pool.
+ *
+ * page_bytes must divide huge_page_bytes, be a multiple of 256, and fit the
+ * divisibility chain of the pool's other views (each level divides the one
+ * above it).  A view whose size is new to the pool can only be created
+ * before any page has been placed (RIMURU_ERR_STATE otherwise); views of an
+ * existing size may be created at any time.
+ */
+int rimuru_view_create(rimuru_pool_t pool, uint64_t page_bytes, rimuru_view_t* out);
+
+/* Destroy a view: frees its pages back to the allocator (merging them) and
+ * its device page table.  The caller must make sure no forward using it is
+ * still running on the GPU. */
+int rimuru_view_destroy(rimuru_view_t view);
+
+/* Pages in the view (pool_bytes / page_bytes) and its page size. */
+int rimuru_view_info(rimuru_view_t view, int64_t* num_pages, uint64_t* page_bytes);
+
+/*
+ * Multi-level page allocator (Rimuru page, abstract: "a multi-level page
+ * allocator that splits and merges pages"; Figure 7; explainer page: a huge
+ * page becomes expert-sized pages and an expert-sized page can become
+ * KV-sized pages, never a huge page straight into KV blocks, and reclaiming
+ * runs the same path in reverse).
+ *
+ * rimuru_page_alloc  hands out the lowest free page of the view's level,
+ *                    splitting the lowest free page of the level above
+ *                    (recursively) when the level has none.
+ *                    RIMURU_ERR_OOM when nothing can be split.
+ * rimuru_page_place  claims one given page id (splitting the pages above it
+ *                    as needed).  RIMURU_ERR_STATE if any page containing it
+ *                    or it itself is owned, or it is already split.
+ * rimuru_page_free   returns a page the view owns; when every sibling cut
+ *                    from the same parent is free they merge back into the
+ *                    parent, recursively.  RIMURU_ERR_STATE if the view does
+ *                    not own it or it is still mapped as an expert
+ *                    projection.
+ * The allocator only places pages: it never reads, writes or moves bytes.
+ */
+int rimuru_page_alloc(rimuru_view_t view, int64_t* page_id);
+int rimuru_page_place(rimuru_view_t view, int64_t page_id);
+int rimuru_page_free(rimuru_view_t view, int64_t page_id);
+
+/* 1 if `page_id` of this view is currently owned by this view, else 0. */
+int rimuru_page_owned(rimuru_view_t view, int64_t page_id, int* owned);
+
+/* ------------------------------------------------------- expert page table */
+
+/*
+ * Declare that `view` holds the experts of an MoE model: `layers` layers of
+ * `experts` experts, hidden size `hidden`, intermediate size `inter`, top
+ * `top_k` routing with renormalised weights when `renorm` != 0.  Creates the
+ * view's expert page table, int32 [layers][experts][3] (all unmapped).
+ * Requirements: hidden and inter multiples of 128, hidden * inter * 2 <=
+ * page_bytes (one projection per page), 1 <= top_k <= min(experts, 32),
+ * experts <= 512.  RIMURU_ERR_UNSUPPORTED otherwise; RIMURU_ERR_STATE if the
+ * view already has a shape.
+ */
+int rimuru_view_set_moe_shape(rimuru_view_t view, int layers, int experts, int hidden, int inter,
+                              int top_k, int renorm);
+
+/*
+ * Expert page table entry (explainer page: each tensor type gets "its own
+ * page table"; the page-table-aware kernel reads expert pages where they
+ * sit).  Maps projection `proj` (RIMURU_PROJ_W1/W3/W2) of `expert` in
+ * `layer` to page `page_id` of this view, which must be owned by the view.
+ * The projection is stored bf16 row-major starting at the page base: w1 and
+ * w3 as [hidden][inter], w2 as [inter][hidden].
+ * The device copy of the table is refreshed by the next forward call on its
+ * stream; the caller must not call this while a forward that reads the old
+ * entry may still be queued if it relies on the old mapping.
+ */
+int rimuru_expert_map(rimuru_view_t view, int layer, int expert, int proj, int64_t page_id);
+
+/* Clear one entry (the page stays owned by the view). */
+int rimuru_expert_unmap(rimuru_view_t view, int layer, int expert, int proj);
+
+/* Read one entry (-1 if unmapped). */
+int rimuru_expert_lookup(rimuru_view_t view, int layer, int expert, int proj, int64_t* page_id);
+
+/* ---------------------------------------------------------------- forward */
+
+/* Workspace (device bytes) a forward of `num_tokens` tokens needs; 0 on a
+ * bad view.  The workspace holds routing ids/weights, the expert-sorted
+ * permutation, the tile table and the bf16 intermediates. */
+uint64_t rimuru_moe_workspace_bytes(rimuru_view_t view, int num_tokens);
+
+/* Byte offsets of the named regions inside the workspace, for inspection
+ * and tests (all relative to the workspace base).  A = num_tokens * top_k. */
+typedef struct rimuru_ws_layout {
+  uint64_t ids;        /* int32 [A]: expert of assignment f = t*k + j */
+  uint64_t weights;    /* fp32 [A]: routing weight of assignment f */
+  uint64_t chunk_hist; /* int32 [chunks][experts]: per-chunk expert counts */
+  uint64_t offsets;    /* int32 [experts + 1]: expert e owns sorted rows offsets[e] .. offsets[e+1]-1 */
+  uint64_t sorted;     /* int32 [A]: assignment f held by sorted row r (ascending f within an expert) */
+  uint64_t inv;        /* int32 [A]: sorted row of assignment f */
+  uint64_t tiles;      /* int32 [max_tiles][2]: (expert, first sorted row) of each 128-row block */
+  uint64_t num_tiles;  /* int32: number of valid row blocks */
+  uint64_t x_sorted;   /* bf16 [A][hidden]: x rows in sorted order */
+  uint64_t h;          /* bf16 [A][inter]: silu(x w1) * (x w3) in sorted order */
+  uint64_t y;          /* bf16 [A][hidden]: h w2 in sorted order (unweighted) */
+  uint64_t total;      /* bytes needed */
+  int32_t chunks;      /* number of routing chunks */
+  int32_t max_tiles;   /* capacity of the tile table */
+} rimuru_ws_layout;
+
+int rimuru_moe_workspace_layout(rimuru_view_t view, int num_tokens, rimuru_ws_layout* out);
+
+/*
+ * The page-table-aware fused MoE layer (Rimuru page, abstract: "a
+ * page-table-aware fused MoE kernel directly accesses non-contiguous expert
+ * weights, avoiding copy overhead"; explainer page, paragraph on the fused
+ * MoE kernel).  For layer `layer` of `view`:
+ *   routing  ids[t, 0..k-1]: the k largest logits of token t, larger first,
+ *            lower expert index first on equal values; weights w[t, j] =
+ *            softmax probabilities of the chosen experts, divided by their
+ *            sum (renorm) or by the sum over all experts;
+ *   grouping assignments f = t*k + j sorted by expert, ascending f within one
+ *            expert;
+ *   GEMM 1   h = silu(x w1_e) * (x w3_e), w1_e and w3_e read from their pages;
+ *   GEMM 2   y = h w2_e, read from its page;
+ *   combine  out[t] = sum_j w[t, j] * y[t*k + j], j ascending, in fp32.
+ * Arguments:
+ *   x_bf16      device, bf16 [num_tokens][hidden], 16-byte aligned
+ *   logits      device, fp32 [num_tokens][experts], 16-byte aligned, finite
+ *   num_tokens  >= 0 (0 returns at once), <= 1 << 20
+ *   out_bf16    device, bf16 [num_tokens][hidden], 16-byte aligned; may not
+ *               alias x
+ *   workspace   device, >= rimuru_moe_workspace_bytes(view, num_tokens)
+ *               bytes, 1024-byte aligned; contents on return are the
+ *               intermediates described by rimuru_moe_workspace_layout()
+ *   stream      cudaStream_t as void*
+ * Every (layer, expert, projection) of `layer` must be mapped
+ * (RIMURU_ERR_UNMAPPED otherwise).  Host-side checks run before any launch;
+ * kernel-side problems set the device error word and never trap.
+ */
+int rimuru_moe_forward(const void* x_bf16, const float* logits, int num_tokens, rimuru_view_t view,
+                       int layer, void* out_bf16, void* workspace, uint64_t workspace_bytes,
+                       void* stream);
+
+/* Device error word of the view (RIMURU_DEV_*).  Synchronises with the
+ * device (cudaMemcpy) so call it after the forward's stream has been
+ * synchronised; clear != 0 resets it to RIMURU_DEV_OK. */
+int rimuru_get_device_error(rimuru_view_t view, int* code, int clear);
+
+/* ------------------------------------------------------------- profiling */
+
+/* Kernels launched by one forward, in launch order. */
+enum {
+  RIMURU_K_ROUTE = 0,
+  RIMURU_K_ALIGN = 1,
+  RIMURU_K_GATHER = 2,
+  RIMURU_K_GEMM1 = 3,
+  RIMURU_K_GEMM2 = 4,
+  RIMURU_K_COMBINE = 5,
+  RIMURU_K_COUNT = 6
+};
+
+/* Name of kernel slot `k` ("moe_route", ...), or NULL. */
+const char* rimuru_kernel_name(int k);
+
+/* Record a CUDA event pair around every kernel launch of the next
+ * `capacity` forwards of this view (enable != 0), or stop recording.
+ * Enabling resets the records. */
+int rimuru_profile_enable(rimuru_view_t view, int enable, int capacity);
+
+/* Launch count and summed device time (ms) of kernel slot `k` over the
+ * recorded forwards.  Synchronises on the recorded events. */
+int rimuru_profile_read(rimuru_view_t view, int k, int* launches, double* total_ms);
+
+/* Number of SMs the kernels size their persistent grids for (0 if no
+ * device is visible). */
+int rimuru_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RIMURU_H_ */

@@ -1,0 +1,316 @@
+// Paged grouped GEMMs of the fused MoE layer on sm_103a tensor cores.
+//
+// Rimuru (arXiv 2610.40305), abstract: "a page-table-aware fused MoE kernel
+// directly accesses non-contiguous expert weights, avoiding copy overhead";
+// explainer page, paragraph on the fused MoE kernel: an ordinary fused MoE
+// kernel would need an expert's scattered pages copied into one contiguous
+// buffer, this one reads them where they sit.
+//
+// Here that becomes: the expert view is one 3-D TMA tensor map over the whole
+// pool, [pages][rows][cols] with the page stride equal to the view's page
+// size, so "resolve the expert's page through the page table" is the third
+// TMA coordinate = page_table[expert][proj].  No descriptor is rewritten per
+// expert and no byte of a weight is copied anywhere but into shared memory.
+//
+// Tile: 128 assignment rows x 256 MMA columns x 64-deep k blocks.
+//   GEMM 1: columns 0..127 come from the w1 page, 128..255 from the w3 page
+//           (same 128 output columns), so gate and up accumulate side by side
+//           in TMEM and the epilogue writes h = silu(gate) * up in bf16.
+//   GEMM 2: 256 consecutive columns of the w2 page; the epilogue writes y.
+// A (activations, K-major) and B (weights, MN-major: rows of the page are k)
+// are staged by TMA with 128-byte swizzle into a 4-deep ring; one thread
+// issues tcgen05.mma into a double-buffered TMEM accumulator (2 x 256
+// columns) so the epilogue of one tile overlaps the main loop of the next.
+// Warp roles: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
+// warps 2-5 = epilogue (warp w reads TMEM lanes 32 * (w % 4) ..).
+#include "device.cuh"
+#include "kernels.h"
+
+namespace rimuru {
+namespace {
+
+using namespace dev;
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int BN = 256;                      // MMA N
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;         // 16 KiB
+constexpr int kBChunk = BK * 64 * 2;         // 8 KiB: [64 k rows][64 cols] of one page
+constexpr int kBBytes = 4 * kBChunk;         // 32 KiB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 2 * BN;            // two accumulators
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align slack*/ + 256 /*barriers*/;
+
+struct Shared {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <bool kSwiGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
+                      const __grid_constant__ CUtensorMap tm_w, const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  Shared* sh = reinterpret_cast<Shared*>(smem + kStages * kStageBytes);
+  volatile int* abort = &sh->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sh->tfull[a], 1);
+      mbar_init(&sh->tempty[a], 128);
+    }
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tm_act);
+    prefetch_tmap(&tm_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+
+  grid_dep_wait();  // tile table, offsets and activations come from earlier kernels
+  const int n_tiles = *p.num_tiles * p.n_blocks;
+  const int nkb = p.num_k_blocks;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      const uint64_t pol_w = p.weights_evict_first ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_a = policy_evict_last();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+        const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
+        const int e = p.tiles[2 * mb], row0 = p.tiles[2 * mb + 1];
+        int pg0, pg1, n0;
+        if (kSwiGLU) {
+          pg0 = p.page_table[3 * e + RIMURU_PROJ_W1];
+          pg1 = p.page_table[3 * e + RIMURU_PROJ_W3];
+          n0 = nb * (BN / 2);
+        } else {
+          pg0 = pg1 = p.page_table[3 * e + RIMURU_PROJ_W2];
+          n0 = nb * BN;
+        }
+        if (pg0 < 0 || pg0 >= p.num_pages || pg1 < 0 || pg1 >= p.num_pages) {
+          set_error(p.err, RIMURU_DEV_BAD_PAGE);  // host checks make this unreachable
+          pg0 = pg1 = 0;
+        }
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+          if (!mbar_wait(&sh->empty[s], ph ^ 1u, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
+          tma_load_2d(sA + s * kABytes, &tm_act, &sh->full[s], kb * BK, row0, pol_a);
+          uint8_t* b = sB + s * kBBytes;
+          if (kSwiGLU) {
+            tma_load_3d(b + 0 * kBChunk, &tm_w, &sh->full[s], n0, kb * BK, pg0, pol_w);
+            tma_load_3d(b + 1 * kBChunk, &tm_w, &sh->full[s], n0 + 64, kb * BK, pg0, pol_w);
+            tma_load_3d(b + 2 * kBChunk, &tm_w, &sh->full[s], n0, kb * BK, pg1, pol_w);
+            tma_load_3d(b + 3 * kBChunk, &tm_w, &sh->full[s], n0 + 64, kb * BK, pg1, pol_w);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              tma_load_3d(b + c * kBChunk, &tm_w, &sh->full[s], n0 + 64 * c, kb * BK, pg0, pol_w);
+          }
+        }
+      }
+      if (!ok) {
+        set_error(p.err, RIMURU_DEV_TIMEOUT);
+        sh->abort = 1;
+      }
+      // every copy this thread issued must have landed before the CTA exits
+      volatile int never = 0;
+      const uint32_t first = it > static_cast<uint32_t>(kStages) ? it - kStages : 0u;
+      for (uint32_t j = first; j < it; ++j)
+        mbar_wait(&sh->full[j % kStages], (j / kStages) & 1u, &never);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true);
+      uint32_t it = 0, local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++local) {
+        const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
+        if (!mbar_wait(&sh->tempty[acc], aph ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+          if (!mbar_wait(&sh->full[s], ph, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * kABytes);
+          const uint32_t b0 = smem_u32(sB + s * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; +32 B per 16 k.
+            const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+            // B: MN-major, 64-column chunks kBChunk apart (LBO), 8-k-row groups
+            // 1024 B apart (SBO); +16 rows * 128 B per 16 k.
+            const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kBChunk, 1024);
+            umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&sh->empty[s]);  // stage s is free once these MMAs are done
+        }
+        if (!ok) break;
+        umma_commit(&sh->tfull[acc]);  // accumulator ready for the epilogue
+      }
+      if (!ok) {
+        set_error(p.err, RIMURU_DEV_TIMEOUT);
+        sh->abort = 1;
+      }
+      // all MMAs must be finished before TMEM is released
+      umma_commit(&sh->drain);
+      volatile int never = 0;
+      mbar_wait(&sh->drain, 0, &never);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may read
+    const int r = q * 32 + lane;
+    uint32_t local = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+      const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
+      const bool got = mbar_wait(&sh->tfull[acc], aph, abort);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) {
+          set_error(p.err, RIMURU_DEV_TIMEOUT);
+          sh->abort = 1;
+        }
+        break;
+      }
+      tc_fence_after();
+      const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
+      const int e = p.tiles[2 * mb], row0 = p.tiles[2 * mb + 1];
+      const int rows = min(BM, p.offsets[e + 1] - row0);
+      const bool valid = r < rows;
+      __nv_bfloat16* orow = p.out + static_cast<size_t>(row0 + r) * p.ldo;
+      const uint32_t tb = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+      if (kSwiGLU) {
+        const int n0 = nb * (BN / 2);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tb + c0, g);
+          tmem_ld32(tb + BN / 2 + c0, u);
+          tmem_ld_wait();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              o.x = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 0]), __uint_as_float(u[8 * v + 0])),
+                                silu_mul(__uint_as_float(g[8 * v + 1]), __uint_as_float(u[8 * v + 1])));
+              o.y = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 2]), __uint_as_float(u[8 * v + 2])),
+                                silu_mul(__uint_as_float(g[8 * v + 3]), __uint_as_float(u[8 * v + 3])));
+              o.z = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 4]), __uint_as_float(u[8 * v + 4])),
+                                silu_mul(__uint_as_float(g[8 * v + 5]), __uint_as_float(u[8 * v + 5])));
+              o.w = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 6]), __uint_as_float(u[8 * v + 6])),
+                                silu_mul(__uint_as_float(g[8 * v + 7]), __uint_as_float(u[8 * v + 7])));
+              dst[v] = o;
+            }
+          }
+        }
+      } else {
+        const int n0 = nb * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t a[32];
+          tmem_ld32(tb + c0, a);
+          tmem_ld_wait();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              o.x = pack_bf16x2(__uint_as_float(a[8 * v + 0]), __uint_as_float(a[8 * v + 1]));
+              o.y = pack_bf16x2(__uint_as_float(a[8 * v + 2]), __uint_as_float(a[8 * v + 3]));
+              o.z = pack_bf16x2(__uint_as_float(a[8 * v + 4]), __uint_as_float(a[8 * v + 5]));
+              o.w = pack_bf16x2(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7]));
+              dst[v] = o;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sh->tempty[acc]);
+    }
+  }
+
+  grid_dep_launch();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <bool kSwiGLU>
+cudaError_t launch_gemm(const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a,
+                        const LaunchOpts& o) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t st = cudaFuncSetAttribute(paged_gemm_kernel<kSwiGLU>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (st != cudaSuccess) return st;
+    configured = true;
+  }
+  const long long tiles = static_cast<long long>(a.max_tiles) * a.n_blocks;
+  const int grid = static_cast<int>(tiles < o.sm_count ? tiles : o.sm_count);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid > 0 ? grid : 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = o.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = o.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, paged_gemm_kernel<kSwiGLU>, tm_act, tm_w, a);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm1_swiglu(const CUtensorMap& tm_x, const CUtensorMap& tm_w13,
+                                const GemmArgs& a, const LaunchOpts& o) {
+  return launch_gemm<true>(tm_x, tm_w13, a, o);
+}
+
+cudaError_t launch_gemm2(const CUtensorMap& tm_h, const CUtensorMap& tm_w2, const GemmArgs& a,
+                         const LaunchOpts& o) {
+  return launch_gemm<false>(tm_h, tm_w2, a, o);
+}
+
+}  // namespace rimuru

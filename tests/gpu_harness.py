@@ -1,0 +1,77 @@
+"""Runs one forward of the paged fused-MoE layer through the C ABI and returns every
+intermediate the workspace holds (routing ids and weights, offsets, the permutation and
+its inverse, the tile table, x_sorted, h, y) plus the output, all as numpy arrays."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from paged_moe_shared_gb300 import rimuru as R
+from paged_moe_shared_gb300.device_pool import load_workload
+
+DEV = "cuda:0"
+
+
+def bf16_tensor(bits: np.ndarray, device=DEV) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+class Runner:
+    """A workload placed on the device once; ``forward`` can be called repeatedly."""
+
+    def __init__(self, w, device=DEV):
+        self.w = w
+        self.pool, self.ev, self.kv = load_workload(w, device)
+        self.x = bf16_tensor(w.x_bits, device)
+        self.logits = torch.from_numpy(np.ascontiguousarray(w.logits)).to(device)
+        self.out = torch.empty_like(self.x)
+        self.ws_bytes = R.rimuru_moe_workspace_bytes(self.ev, w.T)
+        self.ws_raw = torch.empty(self.ws_bytes + 1024, dtype=torch.uint8, device=device)
+        off = (-self.ws_raw.data_ptr()) % 1024
+        self.ws = self.ws_raw[off:off + self.ws_bytes]
+        self.layout = R.rimuru_moe_workspace_layout(self.ev, w.T)
+
+    def forward(self, stream=None):
+        s = stream if stream is not None else torch.cuda.current_stream()
+        R.rimuru_moe_forward(self.x.data_ptr(), self.logits.data_ptr(), self.w.T, self.ev, 0,
+                             self.out.data_ptr(), self.ws.data_ptr(), self.ws_bytes, s.cuda_stream)
+
+    def region(self, name, dtype, count):
+        off = self.layout[name]
+        nbytes = count * torch.tensor([], dtype=dtype).element_size()
+        return self.ws[off:off + nbytes].view(dtype)
+
+    def results(self):
+        torch.cuda.synchronize()
+        w = self.w
+        s = w.shape
+        A = w.T * s.k
+        r = {
+            "out": to_f64(self.out),
+            "ids": self.region("ids", torch.int32, A).cpu().numpy().reshape(w.T, s.k),
+            "w": self.region("weights", torch.float32, A).cpu().numpy().reshape(w.T, s.k),
+            "offsets": self.region("offsets", torch.int32, s.E + 1).cpu().numpy(),
+            "sorted": self.region("sorted", torch.int32, A).cpu().numpy(),
+            "inv": self.region("inv", torch.int32, A).cpu().numpy(),
+            "num_tiles": int(self.region("num_tiles", torch.int32, 1).cpu().item()),
+            "h": to_f64(self.region("h", torch.bfloat16, A * s.I).view(A, s.I)),
+            "y": to_f64(self.region("y", torch.bfloat16, A * s.H).view(A, s.H)),
+            "x_sorted": self.region("x_sorted", torch.bfloat16, A * s.H).view(A, s.H),
+            "dev_err": R.rimuru_get_device_error(self.ev, clear=True),
+        }
+        r["tiles"] = self.region("tiles", torch.int32, 2 * r["num_tiles"]).cpu().numpy().reshape(-1, 2)
+        return r
+
+    def close(self):
+        self.pool.close()
+
+
+def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
+    """max |got - ref| / max |ref|; NaN anywhere in got makes it infinite."""
+    if not np.isfinite(got).all():
+        return float("inf")
+    return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30))

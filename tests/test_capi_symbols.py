@@ -1,0 +1,35 @@
+"""librimuru.so loads without a GPU and exports every entry point include/rimuru.h declares."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "rimuru.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rimuru_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_named_entry_points():
+    names = declared_functions()
+    for required in ("rimuru_pool_create", "rimuru_view_create", "rimuru_expert_map",
+                     "rimuru_moe_forward"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    from paged_moe_shared_gb300 import rimuru as R
+    lib = ctypes.CDLL(R.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert missing == []
+    assert sorted(R.EXPORTS) == declared_functions()
+
+
+def test_status_strings():
+    from paged_moe_shared_gb300 import rimuru as R
+    assert R.rimuru_status_string(0) == "RIMURU_OK"
+    assert R.rimuru_status_string(-4) == "RIMURU_ERR_UNMAPPED"
+    assert R.rimuru_kernel_name(R.K_GEMM1) == "moe_gemm1_swiglu"
+    assert R.rimuru_kernel_name(99) is None

@@ -1,0 +1,195 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI.
+
+Bar (from the layer's definition): routing ids, offsets and the expert-sorted permutation
+bit-exact; routing weights within 1e-6; h, y and out within
+max|gpu - oracle| / max|oracle| <= 1e-2 (bf16 inputs and intermediates, fp32 accumulation);
+NaN anywhere counts as a failure.  Every unused pool page holds NaN, so a read outside an
+expert's own pages shows up in the output.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import workloads as wl
+from gpu_harness import Runner, rel_err
+from oracle import Oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+W_TOL = 1e-6
+
+
+@pytest.fixture(scope="module")
+def oracle():
+    return Oracle()
+
+
+def check(res, w, o_res, tokens=None, hidden=True):
+    s = w.shape
+    assert res["dev_err"] == 0, f"device error {res['dev_err']}"
+    np.testing.assert_array_equal(res["ids"], o_res["ids"])
+    assert np.max(np.abs(res["w"] - o_res["w"])) <= W_TOL
+    np.testing.assert_array_equal(res["offsets"], o_res["offsets"])
+    np.testing.assert_array_equal(res["sorted"], o_res["sorted"])
+    A = w.T * s.k
+    assert np.array_equal(res["inv"][res["sorted"]], np.arange(A))
+    counts = np.diff(o_res["offsets"])
+    blocks = (counts + 127) // 128
+    assert res["num_tiles"] == blocks.sum()
+    exp_tiles = [(e, o_res["offsets"][e] + 128 * b) for e in range(s.E) for b in range(blocks[e])]
+    assert [tuple(t) for t in res["tiles"].tolist()] == exp_tiles
+    toks = np.arange(w.T) if tokens is None else np.asarray(tokens)
+    err = rel_err(res["out"][toks], o_res["out"][toks])
+    assert err <= TOL, f"out rel err {err:.3e}"
+    if hidden:
+        rows = np.nonzero(np.isin(res["sorted"] // s.k, toks))[0]
+        f = res["sorted"][rows]
+        eh = rel_err(res["h"][rows], o_res["h"][f])
+        ey = rel_err(res["y"][rows], o_res["y"][f])
+        assert eh <= TOL, f"h rel err {eh:.3e}"
+        assert ey <= TOL, f"y rel err {ey:.3e}"
+    return err
+
+
+def run_oracle(oracle, w, tokens=None, hidden=True):
+    s = w.shape
+    return oracle.moe_forward(w.x_bits, w.logits, w.pool, w.page_bytes, w.page_table, s.H, s.I, s.k,
+                              s.renorm, tokens=tokens, want_hidden=hidden)
+
+
+def run_gpu(w):
+    r = Runner(w)
+    try:
+        r.forward()
+        return r.results()
+    finally:
+        r.close()
+
+
+# ------------------------------------------------------------------ tiny layer
+@pytest.mark.parametrize("seed", range(5))
+def test_tiny(oracle, seed):
+    w = wl.tiny(seed)
+    check(run_gpu(w), w, run_oracle(oracle, w))
+
+
+@pytest.mark.parametrize("T", [1, 2, 13, 300, 1000])
+def test_tiny_ragged_token_counts(oracle, T):
+    """Several 128-row tiles per expert with ragged tails, and single tokens."""
+    w = wl.tiny(7, T=T)
+    check(run_gpu(w), w, run_oracle(oracle, w))
+
+
+@pytest.mark.parametrize("k", [1, 3, 8])
+def test_tiny_top_k(oracle, k):
+    """k = 1 (argmax expert), k = 3, and k = E = 8 (every expert, dense mixture)."""
+    shape = wl.MoEShape(H=256, I=128, E=8, k=k)
+    w = wl.build_simple("tiny_k", shape, 40, pool_pages=64, seed=11)
+    check(run_gpu(w), w, run_oracle(oracle, w))
+
+
+def test_tiny_without_renormalisation(oracle):
+    shape = wl.MoEShape(H=256, I=128, E=8, k=2, renorm=False)
+    w = wl.build_simple("tiny_norenorm", shape, 33, pool_pages=64, seed=12)
+    check(run_gpu(w), w, run_oracle(oracle, w))
+
+
+def test_one_hot_expert_and_empty_experts(oracle):
+    """Every token's first choice is expert 5 (bias), so one expert holds three tiles and
+    several experts get nothing."""
+    shape = wl.TINY
+    x = wl.make_x(13, 300, shape.H)
+    bias = np.zeros(shape.E)
+    bias[5] = 50.0
+    bias[[0, 1, 2]] = -50.0
+    w = wl.build_simple("tiny_hot", shape, 300, pool_pages=64, seed=13, x_bits=x,
+                        logits=wl.make_logits(13, x, shape.E, bias=bias))
+    o = run_oracle(oracle, w)
+    assert np.diff(o["offsets"])[5] == 300 and (np.diff(o["offsets"]) == 0).sum() >= 3
+    check(run_gpu(w), w, o)
+
+
+def test_tied_logits_take_the_lower_index(oracle):
+    """Integer-valued logits with many exact ties."""
+    shape = wl.TINY
+    x = wl.make_x(14, 64, shape.H)
+    logits = np.random.default_rng(14).integers(-1, 2, size=(64, shape.E)).astype(np.float32)
+    w = wl.build_simple("tiny_ties", shape, 64, pool_pages=64, seed=14, x_bits=x, logits=logits)
+    check(run_gpu(w), w, run_oracle(oracle, w))
+
+
+def test_page_placement_does_not_change_the_output():
+    """Same layer, three page placements (and pool sizes): bit-identical GPU output."""
+    shape = wl.TINY
+    weights = wl.make_expert_weights(21, shape)
+    x = wl.make_x(21, 64, shape.H)
+    logits = wl.make_logits(21, x, shape.E)
+    outs = []
+    for seed, pages in ((1, 24), (2, 64), (3, 100)):
+        w = wl.build_simple("tiny_shuffle", shape, 64, pool_pages=pages, seed=seed, weights=weights,
+                            x_bits=x, logits=logits)
+        outs.append(run_gpu(w)["out"])
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_repeated_forwards_are_bitwise_identical():
+    w = wl.tiny(22, T=300)
+    r = Runner(w)
+    try:
+        r.forward()
+        a = r.results()
+        r.forward()
+        r.forward()
+        b = r.results()
+    finally:
+        r.close()
+    for key in ("out", "h", "y", "ids", "w", "sorted", "inv"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_nonfinite_logits_raise_the_device_error():
+    from paged_moe_shared_gb300 import rimuru as R
+    w = wl.tiny(23)
+    w.logits[3, 2] = np.nan
+    res = run_gpu(w)
+    assert res["dev_err"] == R.DEV_NONFINITE
+    assert ((res["ids"] >= 0) & (res["ids"] < w.shape.E)).all()
+
+
+# ------------------------------------------------------------ full-size layers
+@pytest.fixture(scope="module")
+def q3_decode():
+    return wl.q3_decode(0)
+
+
+def test_q3_decode_full(oracle, q3_decode):
+    """Qwen3-30B-A3B-shaped layer, 64 decode tokens, every output element."""
+    w = q3_decode
+    check(run_gpu(w), w, run_oracle(oracle, w))
+
+
+def test_q3_prefill_zipf_sampled(oracle):
+    """8192 prefill tokens with Zipf-skewed routing: routing, permutation and tiles for all
+    tokens; h, y and out for 48 sampled tokens (the oracle computes them one by one)."""
+    w = wl.q3_prefill_zipf(0)
+    tokens = np.sort(np.random.default_rng(0).choice(w.T, 48, replace=False))
+    o = run_oracle(oracle, w, tokens=tokens)
+    counts = np.diff(o["offsets"])
+    assert (counts == 0).sum() >= 1, "Zipf recipe should leave an expert empty"
+    check(run_gpu(w), w, o, tokens=tokens)
+
+
+@pytest.mark.parametrize("T", [1, 16, 256])
+def test_q35_mixed_pool(oracle, T):
+    """Qwen3.5-35B-A3B-shaped layer (256 experts, I = 512) in a pool whose huge pages are
+    partly split into 32 KiB KV blocks full of random data."""
+    w = wl.q35_mixed_pool(0, T=T)
+    check(run_gpu(w), w, run_oracle(oracle, w))
+
+
+def test_q35_mixed_pool_4096_sampled(oracle):
+    w = wl.q35_mixed_pool(0, T=4096)
+    tokens = np.sort(np.random.default_rng(1).choice(w.T, 32, replace=False))
+    check(run_gpu(w), w, run_oracle(oracle, w, tokens=tokens), tokens=tokens)
