@@ -130,6 +130,18 @@ def ncu_traffic(kernel: str, workload: str):
     return rec.get("dram_bytes_per_launch")
 
 
+def make_workload(args):
+    import workloads as wl
+    kw = {"seed": args.seed}
+    if args.tokens is not None:
+        kw["T"] = args.tokens
+    if args.pool_pages is not None:
+        kw["pool_pages"] = args.pool_pages
+    if args.zipf_gamma is not None:
+        kw["gamma"] = args.zipf_gamma
+    return wl.CONFIGS[args.workload](**kw)
+
+
 def kernel_work(w, counts):
     """Algorithmic bytes and flops per launch of each kernel (no padding, no re-reads)."""
     s = w.shape
@@ -163,8 +175,7 @@ def run_ours(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     torch.cuda.set_device(local_rank)
     dev = f"cuda:{local_rank}"
-    w = wl.CONFIGS[args.workload](seed=args.seed) if args.tokens is None else \
-        wl.CONFIGS[args.workload](seed=args.seed, T=args.tokens)
+    w = make_workload(args)
     pool, ev, _ = load_workload(w, dev)
     x = torch.from_numpy(w.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
     logits = torch.from_numpy(w.logits).to(dev)
@@ -254,9 +265,11 @@ def run_ours(args, rank, world, local_rank):
 
     # ---------------------------------------------------------------- roofline
     peaks = load_peaks()
-    decode_like = work["layer"]["flops"] / work["layer"]["bytes"] < 0.5 * (
-        peaks["bf16_tflops_sustained"] * 1e12) / (peaks["hbm_gbs"] * 1e9)
     dom = max(("moe_gemm1_swiglu", "moe_gemm2"), key=lambda n: per_kernel[n]["ms_per_launch"])
+    # the binding roofline of the dominant kernel: whichever of its byte time and its
+    # flop time at the measured peaks is longer
+    decode_like = (work[dom]["bytes"] / (peaks["hbm_gbs"] * 1e9)
+                   >= work[dom]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12))
     t_dom = per_kernel[dom]["ms_per_launch"] / 1e3
     if decode_like:
         achieved = work[dom]["bytes"] / t_dom / 1e9
@@ -347,8 +360,7 @@ def cpu_baseline(w, budget_s):
 
 def run_reference(args):
     import workloads as wl
-    w = wl.CONFIGS[args.workload](seed=args.seed) if args.tokens is None else \
-        wl.CONFIGS[args.workload](seed=args.seed, T=args.tokens)
+    w = make_workload(args)
     n, dt, cores = sample_tokens(w, budget_s=max(2.0, 120.0 / max(args.steps + args.warmup, 1)))
     toks = np.arange(n)
     for _ in range(args.warmup):
@@ -381,6 +393,10 @@ def main():
     ap.add_argument("--workload", default="q3_decode", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--pool-pages", type=int, default=None,
+                    help="pool size in expert pages (q3 workloads; default 1024)")
+    ap.add_argument("--zipf-gamma", type=float, default=None,
+                    help="scale of the Zipf logit bias (q3_prefill_zipf; default 0.5)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-seconds", type=float, default=20.0)

@@ -170,14 +170,32 @@ def test_q3_decode_full(oracle, q3_decode):
     check(run_gpu(w), w, run_oracle(oracle, w))
 
 
+def zipf_exponent(counts, ranks):
+    """Slope of log(count) against log(rank) over the experts that received tokens."""
+    nz = counts > 0
+    return -np.polyfit(np.log(ranks[nz]), np.log(counts[nz]), 1)[0]
+
+
 def test_q3_prefill_zipf_sampled(oracle):
-    """8192 prefill tokens with Zipf-skewed routing: routing, permutation and tiles for all
-    tokens; h, y and out for 48 sampled tokens (the oracle computes them one by one)."""
+    """8192 prefill tokens with Zipf(1.1)-skewed routing: routing, permutation and tiles for
+    all tokens; h, y and out for 48 sampled tokens (the oracle computes them one by one)."""
     w = wl.q3_prefill_zipf(0)
     tokens = np.sort(np.random.default_rng(0).choice(w.T, 48, replace=False))
     o = run_oracle(oracle, w, tokens=tokens)
     counts = np.diff(o["offsets"])
-    assert (counts == 0).sum() >= 1, "Zipf recipe should leave an expert empty"
+    s = zipf_exponent(counts, wl.zipf_ranks(0, w.shape.E))
+    assert 0.9 <= s <= 1.3, f"realised popularity exponent {s:.2f}"
+    check(run_gpu(w), w, o, tokens=tokens)
+
+
+def test_q3_prefill_heavy_skew_sampled(oracle):
+    """A steeper bias (gamma 2): 38 of 128 experts get every assignment, the rest are empty,
+    and the hottest expert holds all 8192 tokens (64 row blocks)."""
+    w = wl.q3_prefill_zipf(0, gamma=2.0)
+    tokens = np.sort(np.random.default_rng(2).choice(w.T, 32, replace=False))
+    o = run_oracle(oracle, w, tokens=tokens)
+    counts = np.diff(o["offsets"])
+    assert (counts == 0).sum() >= 1 and counts.max() == w.T
     check(run_gpu(w), w, o, tokens=tokens)
 
 

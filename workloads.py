@@ -100,9 +100,16 @@ def make_logits(seed: int, x_bits: np.ndarray, E: int, gate_std: float = 0.02,
     return logits.astype(np.float32)
 
 
-def zipf_bias(seed: int, E: int, s: float = 1.1, gamma: float = 2.0) -> np.ndarray:
-    """Per-expert bias b_e = gamma * ln(r_e^-s), r a seeded permutation of ranks 1..E."""
-    r = _rng(seed, "zipf").permutation(E) + 1
+def zipf_ranks(seed: int, E: int) -> np.ndarray:
+    """Popularity rank (1 = most popular) of each expert: a seeded permutation of 1..E."""
+    return _rng(seed, "zipf").permutation(E) + 1
+
+
+def zipf_bias(seed: int, E: int, s: float = 1.1, gamma: float = 0.5) -> np.ndarray:
+    """Per-expert logit bias b_e = gamma * ln(r_e^-s).  With x Wg noise of std ~0.9 and
+    top-8 of 128 experts, gamma = 0.5 makes the realised per-expert assignment counts fall
+    off as rank^-1.1 (fitted exponent ~1.11 at 8192 tokens)."""
+    r = zipf_ranks(seed, E)
     return gamma * (-s) * np.log(r.astype(np.float64))
 
 
@@ -212,14 +219,15 @@ def tiny(seed: int = 0, T: int = 16) -> Workload:
     return build_simple("tiny", TINY, T, pool_pages=64, seed=seed)
 
 
-def q3_decode(seed: int = 0, T: int = 64) -> Workload:
+def q3_decode(seed: int = 0, T: int = 64, pool_pages: int = 1024) -> Workload:
     """Qwen3-30B-A3B-shaped layer, 64 decode tokens; 384 pages of 3 MiB in a 1024-page pool."""
-    return build_simple("q3_decode", Q3, T, pool_pages=1024, seed=seed)
+    return build_simple("q3_decode", Q3, T, pool_pages=pool_pages, seed=seed)
 
 
-def q3_prefill_zipf(seed: int = 0, T: int = 8192, gamma: float = 2.0) -> Workload:
+def q3_prefill_zipf(seed: int = 0, T: int = 8192, gamma: float = 0.5,
+                    pool_pages: int = 1024) -> Workload:
     """Same layer, 8192 prefill tokens, expert popularity skewed by a Zipf(1.1) logit bias."""
-    w = build_simple("q3_prefill_zipf", Q3, T, pool_pages=1024, seed=seed,
+    w = build_simple("q3_prefill_zipf", Q3, T, pool_pages=pool_pages, seed=seed,
                      bias=zipf_bias(seed, Q3.E, 1.1, gamma))
     w.notes["zipf_gamma"] = gamma
     return w
