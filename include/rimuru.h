@@ -79,9 +79,9 @@ const char* rimuru_status_string(int status);
 /* ------------------------------------------------------------------- pool */
 
 /*
- * Shared page pool (Rimuru page, abstract: "a shared page pool" over which
- * heterogeneous tensors share device memory; explainer page: the pool is cut
- * into huge pages).
+ * Shared page pool (Rimuru page, abstract: one pool of device pages that
+ * tensors of different types share; explainer page, memory-manager
+ * paragraph: the pool is cut into huge pages).
  *
  * dev_base          device pointer to `bytes` bytes owned by the caller; must
  *                   be 2 MiB aligned (over-allocate and align up).
@@ -126,9 +126,8 @@ int rimuru_pool_level_stats(rimuru_pool_t pool, int level, rimuru_level_stats* o
 /* ------------------------------------------------------------------ views */
 
 /*
- * Memory view (Rimuru page, abstract and Figure 6 "multi-view memory
- * layout": each tensor type interprets the shared space with its own page
- * size and its own page table).  Page `i` of a view is the byte range
+ * Memory view (Rimuru page, abstract and Figure 6: every tensor type reads
+ * the shared space with a page size and a page table of its own).  Page `i` of a view is the byte range
  * [i * page_bytes, (i + 1) * page_bytes) of the pool.
  *
  * page_bytes must divide huge_page_bytes, be a multiple of 256, and fit the
@@ -148,11 +147,11 @@ int rimuru_view_destroy(rimuru_view_t view);
 int rimuru_view_info(rimuru_view_t view, int64_t* num_pages, uint64_t* page_bytes);
 
 /*
- * Multi-level page allocator (Rimuru page, abstract: "a multi-level page
- * allocator that splits and merges pages"; Figure 7; explainer page: a huge
- * page becomes expert-sized pages and an expert-sized page can become
- * KV-sized pages, never a huge page straight into KV blocks, and reclaiming
- * runs the same path in reverse).
+ * Multi-level page allocator (Rimuru page, abstract, and Figure 7: pages
+ * are cut into smaller pages and joined back; explainer page, memory-manager
+ * paragraph: huge pages are cut into expert-sized pages, expert-sized pages
+ * into KV-sized pages, huge pages never directly into KV blocks, and freeing
+ * walks the same chain upwards).
  *
  * rimuru_page_alloc  hands out the lowest free page of the view's level,
  *                    splitting the lowest free page of the level above
@@ -191,9 +190,9 @@ int rimuru_view_set_moe_shape(rimuru_view_t view, int layers, int experts, int h
                               int top_k, int renorm);
 
 /*
- * Expert page table entry (explainer page: each tensor type gets "its own
- * page table"; the page-table-aware kernel reads expert pages where they
- * sit).  Maps projection `proj` (RIMURU_PROJ_W1/W3/W2) of `expert` in
+ * Expert page table entry (explainer page, memory-manager paragraph: each
+ * tensor type keeps a page table of its own; paragraph on the fused MoE
+ * kernel: the kernel reads an expert's pages in place).  Maps projection `proj` (RIMURU_PROJ_W1/W3/W2) of `expert` in
  * `layer` to page `page_id` of this view, which must be owned by the view.
  * The projection is stored bf16 row-major starting at the page base: w1 and
  * w3 as [hidden][inter], w2 as [inter][hidden].
@@ -238,10 +237,9 @@ typedef struct rimuru_ws_layout {
 int rimuru_moe_workspace_layout(rimuru_view_t view, int num_tokens, rimuru_ws_layout* out);
 
 /*
- * The page-table-aware fused MoE layer (Rimuru page, abstract: "a
- * page-table-aware fused MoE kernel directly accesses non-contiguous expert
- * weights, avoiding copy overhead"; explainer page, paragraph on the fused
- * MoE kernel).  For layer `layer` of `view`:
+ * The page-table-aware fused MoE layer (Rimuru page, abstract: the MoE
+ * kernel reads expert weights from scattered pages directly, so nothing is
+ * copied first; explainer page, paragraph on the fused MoE kernel).  For layer `layer` of `view`:
  *   routing  ids[t, 0..k-1]: the k largest logits of token t, larger first,
  *            lower expert index first on equal values; weights w[t, j] =
  *            softmax probabilities of the chosen experts, divided by their

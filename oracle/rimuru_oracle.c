@@ -15,7 +15,7 @@
  *   1. each expert projection is read from one page of the expert memory
  *      view: bytes [page_id * page_bytes, page_id * page_bytes + rows*cols*2)
  *      of the shared pool, bf16, row-major [rows][cols]
- *      (memory views: abstract; Figure 6 "multi-view memory layout");
+ *      (memory views: abstract; Figure 6);
  *      w1, w3 are [H][I] and w2 is [I][H] (Table 1, taken literally);
  *   2. routing: the k largest router logits, larger value first, lower expert
  *      index first among equal values; weights are softmax probabilities of the

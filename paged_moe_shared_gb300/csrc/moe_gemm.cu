@@ -1,16 +1,16 @@
 // Paged grouped GEMMs of the fused MoE layer on sm_103a tensor cores.
 //
-// Rimuru (arXiv 2610.40305), abstract: "a page-table-aware fused MoE kernel
-// directly accesses non-contiguous expert weights, avoiding copy overhead";
-// explainer page, paragraph on the fused MoE kernel: an ordinary fused MoE
-// kernel would need an expert's scattered pages copied into one contiguous
-// buffer, this one reads them where they sit.
+// Rimuru (arXiv 2610.40305), abstract and the explainer page's paragraph on
+// the fused MoE kernel: the MoE kernel reads each expert's weights from the
+// scattered pages of the pool directly, instead of first copying them into a
+// contiguous buffer as an ordinary fused MoE kernel would need.
 //
 // Here that becomes: the expert view is one 3-D TMA tensor map over the whole
 // pool, [pages][rows][cols] with the page stride equal to the view's page
-// size, so "resolve the expert's page through the page table" is the third
-// TMA coordinate = page_table[expert][proj].  No descriptor is rewritten per
-// expert and no byte of a weight is copied anywhere but into shared memory.
+// size, so resolving the expert's page through the page table means setting
+// the third TMA coordinate to page_table[expert][proj].  No descriptor is
+// rewritten per expert and no weight byte is copied anywhere but into shared
+// memory.
 //
 // Tile: 128 assignment rows x 256 MMA columns x 64-deep k blocks.
 //   GEMM 1: columns 0..127 come from the w1 page, 128..255 from the w3 page

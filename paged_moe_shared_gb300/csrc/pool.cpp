@@ -3,12 +3,11 @@
 //
 // Rimuru page (arXiv 2610.40305), abstract: a shared page pool, memory views
 // with their own page size and page table, huge-page alignment and a
-// multi-level page allocator that splits and merges pages; Figure 7
-// ("multi-level page allocation and subdivision").  Explainer page,
-// memory-manager paragraph: huge pages are the LCM of the expert and SSM page
-// sizes; a huge page is split into expert-sized pages and an expert-sized page
-// into KV-sized pages, never a huge page directly into KV blocks; reclaiming
-// runs the same path in reverse.
+// multi-level page allocator that cuts pages and joins them back; Figure 7.
+// Explainer page, memory-manager paragraph: huge pages are the LCM of the
+// expert and SSM page sizes; a huge page is split into expert-sized pages and
+// an expert-sized page into KV-sized pages, never a huge page directly into KV
+// blocks; freeing walks the same chain back up.
 #include <algorithm>
 #include <cstring>
 #include <limits>

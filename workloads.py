@@ -5,8 +5,8 @@ shared pool.  It holds none of the layer's arithmetic (no routing, no GEMM, no
 activation, no combine), so both the CPU oracle and the CUDA path can take their
 inputs from it without sharing any of the method.
 
-Shapes follow Table 1 of the Rimuru page ("Tensor heterogeneity in representative
-modern LLMs"): Qwen3-30B-A3B experts w1, w3 [2048, 768] and w2 [768, 2048];
+Shapes follow Table 1 of the Rimuru page (per-expert projection, KV and state shapes of
+two models): Qwen3-30B-A3B experts w1, w3 [2048, 768] and w2 [768, 2048];
 Qwen3.5-35B-A3B experts w1, w3 [2048, 512], w2 [512, 2048]; KV [2, 4, 128] per
 token.  Pages of the pool follow the explainer's description of memory views
 (one page size and one page table per tensor type over one shared pool) and of
