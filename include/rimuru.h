@@ -267,6 +267,41 @@ int rimuru_moe_forward(const void* x_bf16, const float* logits, int num_tokens, 
                        int layer, void* out_bf16, void* workspace, uint64_t workspace_bytes,
                        void* stream);
 
+/*
+ * The same layer as rimuru_moe_forward, for callers that cannot allocate
+ * device memory.  The Rimuru pages have no counterpart of this entry point.
+ *
+ * Who needs it: a serving engine that hands nearly all device memory to its
+ * own page pool at start-up (as a unified pool does) has nothing left for a
+ * per-call cudaMalloc, and a host that accounts for every device byte itself
+ * may not let a library allocate behind its back; cudaMalloc/cudaFree can
+ * also synchronise the device, which a decode loop cannot afford.  Such a
+ * caller passes only inputs and outputs here.
+ *
+ * Scratch: a fixed array of 16 MiB in the library's device memory (a
+ * file-scope __device__ array), present on every GPU that loads the library
+ * until the process exits.  It holds the routing tables, the sorted
+ * activations, h, y, this layer's page table and an error word; the call
+ * makes no cudaMalloc, cudaFree, cudaMallocHost or other allocating call.
+ * A forward whose workspace (rimuru_moe_workspace_bytes) plus 8.25 KiB does
+ * not fit is rejected with RIMURU_ERR_WORKSPACE before anything is launched
+ * (about 200 tokens at hidden 2048 / inter 768 / top-8).
+ * First call on a device: it looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and caches it; make that
+ * first call before any stream capture.
+ * Sharing: every call uses the same array and finds the previous call's
+ * contents there (the kernels overwrite what they read; the error word is
+ * cleared per call).  Calls whose kernels overlap on the GPU race on the
+ * array: serialise them (one stream, or synchronise between streams).
+ * Arguments are those of rimuru_moe_forward without the workspace, plus
+ * dev_error: an optional device int that receives the first RIMURU_DEV_*
+ * code a kernel reports (the caller zeroes it); NULL keeps errors in the
+ * scratch, where they are not reported.
+ */
+int rimuru_moe_forward_noalloc(const void* x_bf16, const float* logits, int num_tokens,
+                               rimuru_view_t view, int layer, void* out_bf16, int* dev_error,
+                               void* stream);
+
 /* Device error word of the view (RIMURU_DEV_*).  Synchronises with the
  * device (cudaMemcpy) so call it after the forward's stream has been
  * synchronised; clear != 0 resets it to RIMURU_DEV_OK. */

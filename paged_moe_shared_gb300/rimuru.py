@@ -37,6 +37,7 @@ EXPORTS = [
     "rimuru_page_place", "rimuru_page_free", "rimuru_page_owned", "rimuru_view_set_moe_shape",
     "rimuru_expert_map", "rimuru_expert_unmap", "rimuru_expert_lookup",
     "rimuru_moe_workspace_bytes", "rimuru_moe_workspace_layout", "rimuru_moe_forward",
+    "rimuru_moe_forward_noalloc",
     "rimuru_get_device_error", "rimuru_kernel_name", "rimuru_profile_enable",
     "rimuru_profile_read", "rimuru_device_sm_count",
 ]
@@ -87,6 +88,7 @@ def _load():
         "rimuru_moe_workspace_bytes": ([P, i32], u64),
         "rimuru_moe_workspace_layout": ([P, i32, ctypes.POINTER(WsLayout)], i32),
         "rimuru_moe_forward": ([P, P, i32, P, i32, P, P, u64, P], i32),
+        "rimuru_moe_forward_noalloc": ([P, P, i32, P, i32, P, P, P], i32),
         "rimuru_get_device_error": ([P, ctypes.POINTER(i32), i32], i32),
         "rimuru_kernel_name": ([i32], ctypes.c_char_p),
         "rimuru_profile_enable": ([P, i32, i32], i32),
@@ -220,6 +222,17 @@ def rimuru_moe_forward(x_ptr: int, logits_ptr: int, num_tokens: int, view, layer
                                   view, layer, ctypes.c_void_p(out_ptr),
                                   ctypes.c_void_p(workspace_ptr), workspace_bytes,
                                   ctypes.c_void_p(stream)))
+
+
+def rimuru_moe_forward_noalloc(x_ptr: int, logits_ptr: int, num_tokens: int, view, layer: int,
+                               out_ptr: int, dev_error_ptr: int = 0, stream: int = 0) -> None:
+    """The forward without a workspace, for callers that cannot allocate device memory:
+    scratch comes from the library's built-in 16 MiB device array.  ``dev_error_ptr`` is an
+    optional device int32 address that receives the first kernel error code."""
+    _check(lib.rimuru_moe_forward_noalloc(ctypes.c_void_p(x_ptr), ctypes.c_void_p(logits_ptr),
+                                          num_tokens, view, layer, ctypes.c_void_p(out_ptr),
+                                          ctypes.c_void_p(dev_error_ptr or None),
+                                          ctypes.c_void_p(stream)))
 
 
 def rimuru_get_device_error(view, clear: bool = False) -> int:
