@@ -323,13 +323,16 @@ enum {
 /* Name of kernel slot `k` ("moe_route", ...), or NULL. */
 const char* rimuru_kernel_name(int k);
 
-/* Record a CUDA event pair around every kernel launch of the next
- * `capacity` forwards of this view (enable != 0), or stop recording.
- * Enabling resets the records. */
-int rimuru_profile_enable(rimuru_view_t view, int enable, int capacity);
+/* Record a CUDA event pair around the launches of the kernels selected by
+ * `kernel_mask` (bit RIMURU_K_* set) in the next `capacity` forwards of this
+ * view; kernel_mask == 0 stops recording.  Enabling resets the records.  An
+ * event pair between two kernels keeps the second from overlapping the
+ * first, so bracket only the kernels being measured. */
+int rimuru_profile_enable(rimuru_view_t view, int kernel_mask, int capacity);
 
 /* Launch count and summed device time (ms) of kernel slot `k` over the
- * recorded forwards.  Synchronises on the recorded events. */
+ * recorded forwards (0 launches if `k` was not selected).  Synchronises on
+ * the recorded events. */
 int rimuru_profile_read(rimuru_view_t view, int k, int* launches, double* total_ms);
 
 /* Number of SMs the kernels size their persistent grids for (0 if no

@@ -25,6 +25,7 @@ struct DeviceState {
   CUtensorMap tm_w2{};   // [pages][inter][hidden] over the pool
   // profiling: per recorded forward, per kernel, a start/stop event pair
   bool prof_on = false;
+  unsigned prof_mask = 0;  // kernels bracketed by an event pair
   int prof_cap = 0;
   int prof_calls = 0;
   std::vector<cudaEvent_t> prof_ev;
@@ -34,40 +35,6 @@ namespace {
 
 std::string cuda_msg(const char* what, cudaError_t e) {
   return std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
-}
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// bf16 tensor map with 128-byte swizzle; dims/strides innermost first,
-// strides in bytes for dims 1.. (rank - 1).
-int make_map(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims,
-             const cuuint64_t* strides, const cuuint32_t* box) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return fail(RIMURU_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), base, dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(RIMURU_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
-  return RIMURU_OK;
 }
 
 int sm_count_of(int device) {
@@ -85,7 +52,7 @@ uint64_t align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
 
 void layout_for(const View& v, int T, rimuru_ws_layout* L) {
   const uint64_t A = static_cast<uint64_t>(T) * v.top_k;
-  const int tpc = kChunkAssign / v.top_k;
+  const int tpc = tokens_per_chunk(v.top_k);
   const int chunks = T > 0 ? (T + tpc - 1) / tpc : 0;
   const uint64_t max_tiles = (A + kTileM - 1) / kTileM + (A < static_cast<uint64_t>(v.experts) ? A : v.experts);
   uint64_t at = 0;
@@ -128,14 +95,8 @@ int ensure_device_state(View* v) {
   }
   v->dev = d;
   // the expert view as two 3-D tensor maps over the whole pool
-  const uint64_t H = v->hidden, I = v->inter, P = v->n_pages;
-  cuuint64_t dims13[3] = {I, H, P};
-  cuuint64_t str13[2] = {I * 2, v->page_bytes};
-  cuuint64_t dims2[3] = {H, I, P};
-  cuuint64_t str2[2] = {H * 2, v->page_bytes};
-  cuuint32_t box[3] = {64, 64, 1};
-  int st = make_map(&d->tm_w13, v->pool->base, 3, dims13, str13, box);
-  if (st == RIMURU_OK) st = make_map(&d->tm_w2, v->pool->base, 3, dims2, str2, box);
+  int st = make_weight_maps(v->pool->base, v->page_bytes, v->n_pages, v->hidden, v->inter,
+                            &d->tm_w13, &d->tm_w2);
   if (st != RIMURU_OK) {
     std::string msg = rimuru_last_error();
     destroy_device_state(v);
@@ -257,99 +218,32 @@ int rimuru_moe_forward(const void* x_bf16, const float* logits, int num_tokens, 
   st = rimuru::upload_table(&v, stream);
   if (st != RIMURU_OK) return st;
 
-  const int T = num_tokens, E = v.experts, k = v.top_k, H = v.hidden, I = v.inter;
-  const int A = T * k;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  auto* ids = reinterpret_cast<int32_t*>(ws + L.ids);
-  auto* w = reinterpret_cast<float*>(ws + L.weights);
-  auto* chunk_hist = reinterpret_cast<int32_t*>(ws + L.chunk_hist);
-  auto* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
-  auto* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
-  auto* inv = reinterpret_cast<int32_t*>(ws + L.inv);
-  auto* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
-  auto* num_tiles = reinterpret_cast<int32_t*>(ws + L.num_tiles);
-  auto* xs = reinterpret_cast<__nv_bfloat16*>(ws + L.x_sorted);
-  auto* h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
-  auto* y = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
-
-  // activation maps: x_sorted [A][H] and h [A][I], 64 x 128 boxes
-  CUtensorMap tm_x, tm_h;
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(A)};
-    cuuint64_t str[1] = {static_cast<cuuint64_t>(H) * 2};
-    cuuint32_t box[2] = {64, 128};
-    st = rimuru::make_map(&tm_x, xs, 2, dims, str, box);
-    if (st != RIMURU_OK) return st;
-  }
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(I), static_cast<cuuint64_t>(A)};
-    cuuint64_t str[1] = {static_cast<cuuint64_t>(I) * 2};
-    cuuint32_t box[2] = {64, 128};
-    st = rimuru::make_map(&tm_h, h, 2, dims, str, box);
-    if (st != RIMURU_OK) return st;
-  }
-
-  rimuru::LaunchOpts o;
-  o.stream = stream;
-  o.sm_count = rimuru::sm_count_of(d->device);
-  if (o.sm_count <= 0) return fail(RIMURU_ERR_CUDA, "could not query the SM count");
-
-  // per-kernel timing
-  cudaEvent_t* ev = nullptr;
+  rimuru::LayerLaunch a;
+  a.x = x_bf16;
+  a.logits = logits;
+  a.out = out_bf16;
+  a.T = num_tokens;
+  a.E = v.experts;
+  a.k = v.top_k;
+  a.H = v.hidden;
+  a.I = v.inter;
+  a.renorm = v.renorm;
+  a.num_pages = static_cast<int>(v.n_pages);
+  a.ws = static_cast<uint8_t*>(workspace);
+  a.layout = L;
+  a.table = d->d_table + static_cast<size_t>(layer) * v.experts * 3;
+  a.err = d->d_err;
+  a.tm_w13 = &d->tm_w13;
+  a.tm_w2 = &d->tm_w2;
+  a.stream = stream;
+  a.sm_count = rimuru::sm_count_of(d->device);
+  if (a.sm_count <= 0) return fail(RIMURU_ERR_CUDA, "could not query the SM count");
   if (d->prof_on && d->prof_calls < d->prof_cap) {
-    ev = &d->prof_ev[static_cast<size_t>(d->prof_calls) * RIMURU_K_COUNT * 2];
+    a.ev = &d->prof_ev[static_cast<size_t>(d->prof_calls) * RIMURU_K_COUNT * 2];
+    a.ev_mask = d->prof_mask;
     d->prof_calls += 1;
   }
-  cudaError_t e = cudaSuccess;
-  auto mark = [&](int kidx, int which) {
-    if (ev && e == cudaSuccess) e = cudaEventRecord(ev[kidx * 2 + which], stream);
-  };
-
-  const int tpc = rimuru::kChunkAssign / k;
-  rimuru::GemmArgs g1{};
-  g1.page_table = d->d_table + static_cast<size_t>(layer) * E * 3;
-  g1.tiles = tiles;
-  g1.num_tiles = num_tiles;
-  g1.offsets = offsets;
-  g1.num_pages = static_cast<int>(v.n_pages);
-  g1.max_tiles = L.max_tiles;
-  g1.weights_evict_first = (A <= E * rimuru::kTileM / 4) ? 1 : 0;
-  g1.err = d->d_err;
-  rimuru::GemmArgs g2 = g1;
-  g1.out = h;
-  g1.ldo = I;
-  g1.n_blocks = I / 128;
-  g1.num_k_blocks = H / 64;
-  g2.out = y;
-  g2.ldo = H;
-  g2.n_blocks = H / 256;
-  g2.num_k_blocks = I / 64;
-
-  mark(RIMURU_K_ROUTE, 0);
-  if (e == cudaSuccess)
-    e = rimuru::launch_route(logits, T, E, k, v.renorm, tpc, ids, w, chunk_hist, d->d_err, o);
-  mark(RIMURU_K_ROUTE, 1);
-  mark(RIMURU_K_ALIGN, 0);
-  if (e == cudaSuccess)
-    e = rimuru::launch_align(ids, chunk_hist, L.chunks, A, E, tpc * k, offsets, sorted, inv, tiles,
-                             num_tiles, d->d_err, o);
-  mark(RIMURU_K_ALIGN, 1);
-  mark(RIMURU_K_GATHER, 0);
-  if (e == cudaSuccess)
-    e = rimuru::launch_gather(static_cast<const __nv_bfloat16*>(x_bf16), sorted, A, k, H, xs, o);
-  mark(RIMURU_K_GATHER, 1);
-  mark(RIMURU_K_GEMM1, 0);
-  if (e == cudaSuccess) e = rimuru::launch_gemm1_swiglu(tm_x, d->tm_w13, g1, o);
-  mark(RIMURU_K_GEMM1, 1);
-  mark(RIMURU_K_GEMM2, 0);
-  if (e == cudaSuccess) e = rimuru::launch_gemm2(tm_h, d->tm_w2, g2, o);
-  mark(RIMURU_K_GEMM2, 1);
-  mark(RIMURU_K_COMBINE, 0);
-  if (e == cudaSuccess)
-    e = rimuru::launch_combine(y, inv, w, T, k, H, static_cast<__nv_bfloat16*>(out_bf16), o);
-  mark(RIMURU_K_COMBINE, 1);
-  if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, rimuru::cuda_msg("kernel launch", e));
-  return RIMURU_OK;
+  return rimuru::launch_layer(a);
 }
 
 int rimuru_get_device_error(rimuru_view_t view, int* code, int clear) {
@@ -368,15 +262,17 @@ int rimuru_get_device_error(rimuru_view_t view, int* code, int clear) {
   return RIMURU_OK;
 }
 
-int rimuru_profile_enable(rimuru_view_t view, int enable, int capacity) {
+int rimuru_profile_enable(rimuru_view_t view, int kernel_mask, int capacity) {
   rimuru::clear_error();
   if (!view) return fail(RIMURU_ERR_ARG, "null view");
   rimuru::View& v = view->v;
   if (!v.has_shape) return fail(RIMURU_ERR_STATE, "view has no MoE shape");
+  if (kernel_mask < 0 || kernel_mask >= (1 << RIMURU_K_COUNT))
+    return fail(RIMURU_ERR_ARG, "kernel mask out of range");
   int st = rimuru::ensure_device_state(&v);
   if (st != RIMURU_OK) return st;
   rimuru::DeviceState* d = v.dev;
-  if (!enable) {
+  if (kernel_mask == 0) {
     d->prof_on = false;
     return RIMURU_OK;
   }
@@ -390,6 +286,7 @@ int rimuru_profile_enable(rimuru_view_t view, int enable, int capacity) {
   }
   d->prof_cap = capacity;
   d->prof_calls = 0;
+  d->prof_mask = static_cast<unsigned>(kernel_mask);
   d->prof_on = true;
   return RIMURU_OK;
 }
@@ -403,6 +300,7 @@ int rimuru_profile_read(rimuru_view_t view, int k, int* launches, double* total_
   *total_ms = 0.0;
   if (!v.dev) return RIMURU_OK;
   rimuru::DeviceState* d = v.dev;
+  if (!(d->prof_mask >> k & 1u)) return RIMURU_OK;
   for (int c = 0; c < d->prof_calls; ++c) {
     cudaEvent_t a = d->prof_ev[(static_cast<size_t>(c) * RIMURU_K_COUNT + k) * 2];
     cudaEvent_t b = d->prof_ev[(static_cast<size_t>(c) * RIMURU_K_COUNT + k) * 2 + 1];

@@ -6,12 +6,20 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "../../include/rimuru.h"
+
 namespace rimuru {
 
-constexpr int kChunkAssign = 512;  // assignments per routing chunk (= align CTA size)
-constexpr int kTileM = 128;        // rows (assignments) per GEMM tile
+constexpr int kChunkAssign = 1024;  // most assignments in one routing chunk (= align CTA size)
+constexpr int kRouteWarps = 32;     // tokens per routing chunk: one warp per token
+constexpr int kTileM = 128;         // rows (assignments) per GEMM tile
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
+
+// Tokens routed by one CTA (one warp each); their k assignments form one chunk.
+inline int tokens_per_chunk(int k) {
+  return kRouteWarps * k <= kChunkAssign ? kRouteWarps : kChunkAssign / k;
+}
 
 struct LaunchOpts {
   cudaStream_t stream = nullptr;
@@ -60,5 +68,36 @@ cudaError_t launch_gemm2(const CUtensorMap& tm_h, const CUtensorMap& tm_w2, cons
 // a5: out[t] = sum_j w[t*k+j] * y[inv[t*k+j]], j ascending, fp32 then bf16.
 cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv, const float* w, int T,
                            int k, int H, __nv_bfloat16* out, const LaunchOpts& o);
+
+// bf16 TMA descriptor with 128-byte swizzle (dims and box innermost first,
+// strides in bytes for dims 1..rank-1).  Returns a rimuru status.
+int make_bf16_map(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims,
+                  const cuuint64_t* strides, const cuuint32_t* box);
+// The expert view as two 3-D maps over the whole pool: [pages][H][I] (w1, w3)
+// and [pages][I][H] (w2), 64 x 64 boxes.
+int make_weight_maps(void* pool_base, uint64_t page_bytes, int64_t n_pages, int hidden, int inter,
+                     CUtensorMap* tm_w13, CUtensorMap* tm_w2);
+
+// Everything one forward needs; filled by the entry points.
+struct LayerLaunch {
+  const void* x = nullptr;          // bf16 [T][H]
+  const float* logits = nullptr;    // fp32 [T][E]
+  void* out = nullptr;              // bf16 [T][H]
+  int T = 0, E = 0, k = 0, H = 0, I = 0, renorm = 1, num_pages = 0;
+  uint8_t* ws = nullptr;            // workspace base
+  rimuru_ws_layout layout{};        // region offsets inside ws
+  const int32_t* table = nullptr;   // this layer's page table [E][3] (device)
+  int* err = nullptr;               // device error word
+  const CUtensorMap* tm_w13 = nullptr;
+  const CUtensorMap* tm_w2 = nullptr;
+  cudaStream_t stream = nullptr;
+  int sm_count = 0;
+  bool pdl = true;
+  cudaEvent_t* ev = nullptr;        // 2 * RIMURU_K_COUNT events, or null
+  unsigned ev_mask = 0;             // kernels bracketed by their event pair
+};
+
+// Launch the six kernels of one layer.  Returns a rimuru status.
+int launch_layer(const LayerLaunch& a);
 
 }  // namespace rimuru

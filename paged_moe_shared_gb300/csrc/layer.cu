@@ -1,0 +1,165 @@
+// The launch sequence of one paged fused-MoE layer, shared by every forward
+// entry point: route -> align -> gather -> GEMM 1 + SwiGLU -> GEMM 2 ->
+// combine, all on one stream.  Every kernel after the first is launched with
+// programmatic dependent launch, so its launch and prologue overlap the tail
+// of the kernel before it; each kernel waits (griddepcontrol.wait) before it
+// touches what its predecessor wrote.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+#include "kernels.h"
+
+namespace rimuru {
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+std::string cuda_msg(const char* what, cudaError_t e) {
+  return std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+}
+
+}  // namespace
+
+int make_bf16_map(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims,
+                  const cuuint64_t* strides, const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(RIMURU_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), base, dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(RIMURU_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
+  return RIMURU_OK;
+}
+
+int make_weight_maps(void* pool_base, uint64_t page_bytes, int64_t n_pages, int hidden, int inter,
+                     CUtensorMap* tm_w13, CUtensorMap* tm_w2) {
+  const uint64_t H = hidden, I = inter, P = static_cast<uint64_t>(n_pages);
+  cuuint64_t dims13[3] = {I, H, P};
+  cuuint64_t str13[2] = {I * 2, page_bytes};
+  cuuint64_t dims2[3] = {H, I, P};
+  cuuint64_t str2[2] = {H * 2, page_bytes};
+  cuuint32_t box[3] = {64, 64, 1};
+  int st = make_bf16_map(tm_w13, pool_base, 3, dims13, str13, box);
+  if (st == RIMURU_OK) st = make_bf16_map(tm_w2, pool_base, 3, dims2, str2, box);
+  return st;
+}
+
+int launch_layer(const LayerLaunch& a) {
+  const rimuru_ws_layout& L = a.layout;
+  const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I;
+  const int A = T * k;
+  uint8_t* ws = a.ws;
+  auto* ids = reinterpret_cast<int32_t*>(ws + L.ids);
+  auto* w = reinterpret_cast<float*>(ws + L.weights);
+  auto* chunk_hist = reinterpret_cast<int32_t*>(ws + L.chunk_hist);
+  auto* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  auto* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
+  auto* inv = reinterpret_cast<int32_t*>(ws + L.inv);
+  auto* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
+  auto* num_tiles = reinterpret_cast<int32_t*>(ws + L.num_tiles);
+  auto* xs = reinterpret_cast<__nv_bfloat16*>(ws + L.x_sorted);
+  auto* h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
+  auto* y = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
+
+  // activation maps: x_sorted [A][H] and h [A][I], 64 x 128 boxes
+  CUtensorMap tm_x, tm_h;
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(A)};
+    cuuint64_t str[1] = {static_cast<cuuint64_t>(H) * 2};
+    cuuint32_t box[2] = {64, 128};
+    int st = make_bf16_map(&tm_x, xs, 2, dims, str, box);
+    if (st != RIMURU_OK) return st;
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(I), static_cast<cuuint64_t>(A)};
+    cuuint64_t str[1] = {static_cast<cuuint64_t>(I) * 2};
+    cuuint32_t box[2] = {64, 128};
+    int st = make_bf16_map(&tm_h, h, 2, dims, str, box);
+    if (st != RIMURU_OK) return st;
+  }
+
+  GemmArgs g1{};
+  g1.page_table = a.table;
+  g1.tiles = tiles;
+  g1.num_tiles = num_tiles;
+  g1.offsets = offsets;
+  g1.num_pages = a.num_pages;
+  g1.max_tiles = L.max_tiles;
+  g1.weights_evict_first = (A <= E * kTileM / 4) ? 1 : 0;
+  g1.err = a.err;
+  GemmArgs g2 = g1;
+  g1.out = h;
+  g1.ldo = I;
+  g1.n_blocks = I / 128;
+  g1.num_k_blocks = H / 64;
+  g2.out = y;
+  g2.ldo = H;
+  g2.n_blocks = H / 256;
+  g2.num_k_blocks = I / 64;
+
+  LaunchOpts first;
+  first.stream = a.stream;
+  first.sm_count = a.sm_count;
+  first.pdl = false;  // the first kernel follows whatever the caller queued
+  LaunchOpts next = first;
+  next.pdl = a.pdl;
+
+  cudaError_t e = cudaSuccess;
+  auto mark = [&](int kidx, int which) {
+    if (a.ev && (a.ev_mask >> kidx & 1u) && e == cudaSuccess)
+      e = cudaEventRecord(a.ev[kidx * 2 + which], a.stream);
+  };
+  const int tpc = tokens_per_chunk(k);
+
+  mark(RIMURU_K_ROUTE, 0);
+  if (e == cudaSuccess)
+    e = launch_route(a.logits, T, E, k, a.renorm, tpc, ids, w, chunk_hist, a.err, first);
+  mark(RIMURU_K_ROUTE, 1);
+  mark(RIMURU_K_ALIGN, 0);
+  if (e == cudaSuccess)
+    e = launch_align(ids, chunk_hist, L.chunks, A, E, tpc * k, offsets, sorted, inv, tiles,
+                     num_tiles, a.err, next);
+  mark(RIMURU_K_ALIGN, 1);
+  mark(RIMURU_K_GATHER, 0);
+  if (e == cudaSuccess)
+    e = launch_gather(static_cast<const __nv_bfloat16*>(a.x), sorted, A, k, H, xs, next);
+  mark(RIMURU_K_GATHER, 1);
+  mark(RIMURU_K_GEMM1, 0);
+  if (e == cudaSuccess) e = launch_gemm1_swiglu(tm_x, *a.tm_w13, g1, next);
+  mark(RIMURU_K_GEMM1, 1);
+  mark(RIMURU_K_GEMM2, 0);
+  if (e == cudaSuccess) e = launch_gemm2(tm_h, *a.tm_w2, g2, next);
+  mark(RIMURU_K_GEMM2, 1);
+  mark(RIMURU_K_COMBINE, 0);
+  if (e == cudaSuccess)
+    e = launch_combine(y, inv, w, T, k, H, static_cast<__nv_bfloat16*>(a.out), next);
+  mark(RIMURU_K_COMBINE, 1);
+  if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, cuda_msg("kernel launch", e));
+  return RIMURU_OK;
+}
+
+}  // namespace rimuru

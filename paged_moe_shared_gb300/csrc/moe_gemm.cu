@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = sh->tmem_base;
 
   grid_dep_wait();  // tile table, offsets and activations come from earlier kernels
+  grid_dep_launch();  // the next kernel may be scheduled now; it waits for our completion
   const int n_tiles = *p.num_tiles * p.n_blocks;
   const int nkb = p.num_k_blocks;
 
@@ -267,7 +268,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  grid_dep_launch();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -35,16 +35,31 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
 }
 
 // ----------------------------------------------------------------- route
-// Experts per lane: lane l holds experts l, l + 32, l + 64, ...
+// Order-preserving 32-bit key of a float: a > b as floats iff key(a) > key(b).
+// -0 is folded onto +0 first so the two compare equal, as IEEE says.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u << 1) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// One warp per token.  Lane l holds experts l, l + 32, ... (EPL per lane) as
+// keys; each of the k rounds takes the largest untaken key of the warp with
+// one redux.max and, among lanes holding it, the lowest expert index with one
+// redux.min.  Key 0 marks lanes past E (valid keys are >= key(-inf) > 0).
 template <int EPL>
-__global__ void __launch_bounds__(512) moe_route_kernel(const float* __restrict__ logits, int T,
-                                                        int E, int k, int renorm, int tpc,
-                                                        int32_t* __restrict__ ids,
-                                                        float* __restrict__ w,
-                                                        int32_t* __restrict__ chunk_hist,
-                                                        int* err) {
+__global__ void __launch_bounds__(1024) moe_route_kernel(const float* __restrict__ logits, int T,
+                                                         int E, int k, int renorm, int tpc,
+                                                         int32_t* __restrict__ ids,
+                                                         float* __restrict__ w,
+                                                         int32_t* __restrict__ chunk_hist,
+                                                         int* err) {
   extern __shared__ int s_hist[];  // [E]
   grid_dep_wait();
+  grid_dep_launch();
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -53,52 +68,43 @@ __global__ void __launch_bounds__(512) moe_route_kernel(const float* __restrict_
   const int t_end = min(t_begin + tpc, T);
   for (int t = t_begin + warp; t < t_end; t += nwarps) {
     const float* row = logits + static_cast<size_t>(t) * E;
-    float v[EPL];
+    uint32_t key[EPL];
     bool bad = false;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      int e = lane + 32 * i;
-      float x = -INFINITY;
+      const int e = lane + 32 * i;
+      key[i] = 0u;
       if (e < E) {
-        x = row[e];
+        float x = row[e];
         if (!isfinite(x)) {
           bad = true;
           x = -INFINITY;  // invalid input: rank it last, keep ids valid
         }
+        key[i] = order_key(x);
       }
-      v[i] = x;
     }
     if (__any_sync(kFull, bad) && lane == 0) set_error(err, RIMURU_DEV_NONFINITE);
     uint32_t taken = 0;
-    float m = 0.f, psum = 0.f, my_p = 0.f;
+    float mx = 0.f, psum = 0.f, my_p = 0.f;
     int my_id = 0;
     for (int j = 0; j < k; ++j) {
-      // best untaken expert of this lane: larger logit, then lower index
-      float bv = -INFINITY;
-      int be = INT_MAX;
+      uint32_t bk = 0u, bi = 0xffffffffu;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-          bv = v[i];
-          be = e;
+        if (!((taken >> i) & 1u) && key[i] > bk) {  // strict: lowest index among equals
+          bk = key[i];
+          bi = static_cast<uint32_t>(lane + 32 * i);
         }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        float ov = __shfl_xor_sync(kFull, bv, off);
-        int oe = __shfl_xor_sync(kFull, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if (j == 0) m = (bv == -INFINITY) ? 0.f : bv;  // largest logit of the token
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      float p = expf(bv - m);
+      const uint32_t m = __reduce_max_sync(kFull, bk);
+      const uint32_t win = __reduce_min_sync(kFull, bk == m ? bi : 0xffffffffu);
+      const float v = key_value(m);
+      if (j == 0) mx = (v == -INFINITY) ? 0.f : v;  // largest logit of the token
+      if (static_cast<int>(win & 31u) == lane) taken |= 1u << (win >> 5);
+      const float p = expf(v - mx);
       psum += p;
       if (lane == j) {
-        my_id = be;
+        my_id = static_cast<int>(win);
         my_p = p;
       }
     }
@@ -107,7 +113,7 @@ __global__ void __launch_bounds__(512) moe_route_kernel(const float* __restrict_
       float s = 0.f;
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
-        if (lane + 32 * i < E) s += expf(v[i] - m);
+        if (key[i] != 0u) s += expf(key_value(key[i]) - mx);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
       denom = s;
@@ -121,7 +127,6 @@ __global__ void __launch_bounds__(512) moe_route_kernel(const float* __restrict_
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     chunk_hist[static_cast<size_t>(blockIdx.x) * E + e] = s_hist[e];
-  grid_dep_launch();
 }
 
 // Exclusive prefix sum over the block (one value per thread, blockDim <= 1024).
@@ -152,57 +157,79 @@ __device__ int block_exclusive_scan(int v, int* s_warp) {
 }
 
 // ----------------------------------------------------------------- align
+// One CTA per routing chunk (kChunkAssign threads).  Every CTA sums the chunk
+// histograms (all chunks -> totals, earlier chunks -> this chunk's base per
+// expert), with parts = blockDim / E threads per expert column; CTA 0 also
+// writes the offsets and the 128-row tile table.  Inside the chunk an
+// assignment's rank among same-expert assignments is the number of earlier
+// ones, which keeps the order stable.
 __global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ chunk_hist, int chunks, int A,
     int E, int chunk, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted,
     int32_t* __restrict__ inv, int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles,
     int* err) {
+  __shared__ int s_part_tot[kChunkAssign];
+  __shared__ int s_part_bef[kChunkAssign];
   __shared__ int s_base[kMaxExperts];
   __shared__ int s_ids[kChunkAssign];
   __shared__ int s_warp[32];
   grid_dep_wait();
+  grid_dep_launch();
   const int c = blockIdx.x;
-  const int e = threadIdx.x;  // blockDim == kChunkAssign >= E
-  int tot = 0, before = 0;
-  if (e < E) {
-    for (int cc = 0; cc < chunks; ++cc) {
-      int n = chunk_hist[static_cast<size_t>(cc) * E + e];
-      tot += n;
-      if (cc < c) before += n;
-    }
-  }
-  const int off = block_exclusive_scan(tot, s_warp);
-  if (e < E) s_base[e] = off + before;
-  if (c == 0) {
-    if (e < E) offsets[e] = off;
-    if (e == E - 1) offsets[E] = off + tot;
-    const int nb = (tot + kTileM - 1) / kTileM;
-    const int first = block_exclusive_scan(nb, s_warp);
-    if (e < E) {
-      for (int b = 0; b < nb; ++b) {
-        tiles[2 * (first + b)] = e;
-        tiles[2 * (first + b) + 1] = off + b * kTileM;
+  const int tid = threadIdx.x;
+  const int parts = blockDim.x / E;  // >= 2 since E <= kMaxExperts = blockDim / 2
+  {
+    const int e = tid % E, part = tid / E;
+    int tot = 0, bef = 0;
+    if (part < parts) {
+      for (int cc = part; cc < chunks; cc += parts) {
+        const int n = chunk_hist[static_cast<size_t>(cc) * E + e];
+        tot += n;
+        if (cc < c) bef += n;
       }
     }
-    if (e == E - 1) *num_tiles = first + nb;
+    s_part_tot[tid] = tot;
+    s_part_bef[tid] = bef;
   }
   const int f0 = c * chunk;
   const int n = min(chunk, A - f0);
-  if (static_cast<int>(threadIdx.x) < n) s_ids[threadIdx.x] = ids[f0 + threadIdx.x];
+  if (tid < n) s_ids[tid] = ids[f0 + tid];
   __syncthreads();
-  if (static_cast<int>(threadIdx.x) < n) {
-    const int my = s_ids[threadIdx.x];
+  int tot = 0, before = 0;
+  if (tid < E) {
+    for (int p = 0; p < parts; ++p) {
+      tot += s_part_tot[p * E + tid];
+      before += s_part_bef[p * E + tid];
+    }
+  }
+  const int off = block_exclusive_scan(tot, s_warp);
+  if (tid < E) s_base[tid] = off + before;
+  if (c == 0) {
+    if (tid < E) offsets[tid] = off;
+    if (tid == E - 1) offsets[E] = off + tot;
+    const int nb = (tot + kTileM - 1) / kTileM;
+    const int first = block_exclusive_scan(nb, s_warp);
+    if (tid < E) {
+      for (int b = 0; b < nb; ++b) {
+        tiles[2 * (first + b)] = tid;
+        tiles[2 * (first + b) + 1] = off + b * kTileM;
+      }
+    }
+    if (tid == E - 1) *num_tiles = first + nb;
+  }
+  __syncthreads();
+  if (tid < n) {
+    const int my = s_ids[tid];
     if (my < 0 || my >= E) {
       set_error(err, RIMURU_DEV_BAD_SHAPE);
     } else {
       int rank = 0;  // earlier assignments of the same expert inside this chunk
-      for (int j = 0; j < static_cast<int>(threadIdx.x); ++j) rank += (s_ids[j] == my);
+      for (int j = 0; j < tid; ++j) rank += (s_ids[j] == my);
       const int pos = s_base[my] + rank;
-      sorted[pos] = f0 + threadIdx.x;
-      inv[f0 + threadIdx.x] = pos;
+      sorted[pos] = f0 + tid;
+      inv[f0 + tid] = pos;
     }
   }
-  grid_dep_launch();
 }
 
 // ----------------------------------------------------------------- gather
@@ -210,36 +237,53 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict
                                                          const int32_t* __restrict__ sorted, int A,
                                                          int k, int H8, uint4* __restrict__ xs) {
   grid_dep_wait();
+  grid_dep_launch();
   for (int r = blockIdx.x; r < A; r += gridDim.x) {
     const int t = sorted[r] / k;
     const uint4* src = x + static_cast<size_t>(t) * H8;
     uint4* dst = xs + static_cast<size_t>(r) * H8;
     for (int c = threadIdx.x; c < H8; c += blockDim.x) dst[c] = src[c];
   }
-  grid_dep_launch();
 }
 
 // ----------------------------------------------------------------- combine
+// out[t] = sum_j w[t*k+j] * y[inv[t*k+j]], j ascending, fp32, bf16 result.
+// Each thread owns one 16-byte column slice of a token and issues the loads of
+// up to eight slots before it accumulates them in slot order.
 __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restrict__ y,
                                                           const int32_t* __restrict__ inv,
                                                           const float* __restrict__ w, int T,
                                                           int k, int H8, uint4* __restrict__ out) {
   grid_dep_wait();
+  grid_dep_launch();
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     for (int c = threadIdx.x; c < H8; c += blockDim.x) {
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int j = 0; j < k; ++j) {
-        const int f = t * k + j;
-        const float wj = w[f];
-        uint4 v = y[static_cast<size_t>(inv[f]) * H8 + c];
-        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+      for (int j0 = 0; j0 < k; j0 += 8) {
+        uint4 v[8];
+        float wj[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float2 f2 = __bfloat1622float2(p[i]);
-          acc[2 * i] = fmaf(wj, f2.x, acc[2 * i]);
-          acc[2 * i + 1] = fmaf(wj, f2.y, acc[2 * i + 1]);
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          if (j < k) {
+            const int f = t * k + j;
+            wj[jj] = w[f];
+            v[jj] = y[static_cast<size_t>(inv[f]) * H8 + c];
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          if (j0 + jj < k) {
+            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[jj]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f2 = __bfloat1622float2(p[i]);
+              acc[2 * i] = fmaf(wj[jj], f2.x, acc[2 * i]);
+              acc[2 * i + 1] = fmaf(wj[jj], f2.y, acc[2 * i + 1]);
+            }
+          }
         }
       }
       uint4 o;
@@ -250,7 +294,6 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restric
       out[static_cast<size_t>(t) * H8 + c] = o;
     }
   }
-  grid_dep_launch();
 }
 
 }  // namespace
@@ -260,7 +303,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
                          const LaunchOpts& o) {
   const int chunks = (T + tpc - 1) / tpc;
   const size_t smem = static_cast<size_t>(E) * sizeof(int);
-  const dim3 grid(chunks), block(512);
+  const dim3 grid(chunks), block(32 * tpc < 1024 ? 32 * tpc : 1024);
   if (E <= 32)
     return launch(moe_route_kernel<1>, grid, block, smem, o, logits, T, E, k, renorm, tpc, ids, w,
                   chunk_hist, err);

@@ -51,33 +51,6 @@ int scratch_for_device(int device, uint8_t** out) {
   return RIMURU_OK;
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-int encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-           const cuuint32_t* box) {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  if (!fn) return fail(RIMURU_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), base, dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(RIMURU_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
-  return RIMURU_OK;
-}
-
 }  // namespace
 }  // namespace rimuru
 
@@ -131,7 +104,6 @@ extern "C" int rimuru_moe_forward_noalloc(const void* x_bf16, const float* logit
   uint8_t* ws = scratch + kErrBytes + kTableBytes;  // 256-byte aligned base
 
   const int T = num_tokens, E = v.experts, k = v.top_k, H = v.hidden, I = v.inter;
-  const int A = T * k;
   // Left over from the previous call: the scratch error word (cleared here) and
   // the page table (this layer's entries are copied in on every call).  Every
   // other region is written by a kernel before it is read.
@@ -141,79 +113,28 @@ extern "C" int rimuru_moe_forward_noalloc(const void* x_bf16, const float* logit
                         static_cast<size_t>(E) * 3 * sizeof(int32_t), cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, msg_of("scratch set-up", e));
 
-  auto* ids = reinterpret_cast<int32_t*>(ws + L.ids);
-  auto* w = reinterpret_cast<float*>(ws + L.weights);
-  auto* chunk_hist = reinterpret_cast<int32_t*>(ws + L.chunk_hist);
-  auto* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
-  auto* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
-  auto* inv = reinterpret_cast<int32_t*>(ws + L.inv);
-  auto* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
-  auto* num_tiles = reinterpret_cast<int32_t*>(ws + L.num_tiles);
-  auto* xs = reinterpret_cast<__nv_bfloat16*>(ws + L.x_sorted);
-  auto* h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
-  auto* y = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
+  CUtensorMap tm_w13, tm_w2;
+  st = make_weight_maps(v.pool->base, v.page_bytes, v.n_pages, H, I, &tm_w13, &tm_w2);
+  if (st != RIMURU_OK) return st;
 
-  // TMA descriptors: activations in the scratch, expert view over the pool.
-  CUtensorMap tm_x, tm_h, tm_w13, tm_w2;
-  const uint64_t P = static_cast<uint64_t>(v.n_pages);
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(A)};
-    cuuint64_t str[1] = {static_cast<cuuint64_t>(H) * 2};
-    cuuint32_t box[2] = {64, 128};
-    if ((st = encode(&tm_x, xs, 2, dims, str, box)) != RIMURU_OK) return st;
-  }
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(I), static_cast<cuuint64_t>(A)};
-    cuuint64_t str[1] = {static_cast<cuuint64_t>(I) * 2};
-    cuuint32_t box[2] = {64, 128};
-    if ((st = encode(&tm_h, h, 2, dims, str, box)) != RIMURU_OK) return st;
-  }
-  {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(I), static_cast<cuuint64_t>(H), P};
-    cuuint64_t str[2] = {static_cast<cuuint64_t>(I) * 2, v.page_bytes};
-    cuuint32_t box[3] = {64, 64, 1};
-    if ((st = encode(&tm_w13, v.pool->base, 3, dims, str, box)) != RIMURU_OK) return st;
-  }
-  {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(I), P};
-    cuuint64_t str[2] = {static_cast<cuuint64_t>(H) * 2, v.page_bytes};
-    cuuint32_t box[3] = {64, 64, 1};
-    if ((st = encode(&tm_w2, v.pool->base, 3, dims, str, box)) != RIMURU_OK) return st;
-  }
-
-  LaunchOpts o;
-  o.stream = stream;
-  o.sm_count = sms;
-  const int tpc = kChunkAssign / k;
-  GemmArgs g1{};
-  g1.page_table = table;
-  g1.tiles = tiles;
-  g1.num_tiles = num_tiles;
-  g1.offsets = offsets;
-  g1.num_pages = static_cast<int>(v.n_pages);
-  g1.max_tiles = L.max_tiles;
-  g1.weights_evict_first = (A <= E * kTileM / 4) ? 1 : 0;
-  g1.err = err;
-  GemmArgs g2 = g1;
-  g1.out = h;
-  g1.ldo = I;
-  g1.n_blocks = I / 128;
-  g1.num_k_blocks = H / 64;
-  g2.out = y;
-  g2.ldo = H;
-  g2.n_blocks = H / 256;
-  g2.num_k_blocks = I / 64;
-
-  e = launch_route(logits, T, E, k, v.renorm, tpc, ids, w, chunk_hist, err, o);
-  if (e == cudaSuccess)
-    e = launch_align(ids, chunk_hist, L.chunks, A, E, tpc * k, offsets, sorted, inv, tiles,
-                     num_tiles, err, o);
-  if (e == cudaSuccess)
-    e = launch_gather(static_cast<const __nv_bfloat16*>(x_bf16), sorted, A, k, H, xs, o);
-  if (e == cudaSuccess) e = launch_gemm1_swiglu(tm_x, tm_w13, g1, o);
-  if (e == cudaSuccess) e = launch_gemm2(tm_h, tm_w2, g2, o);
-  if (e == cudaSuccess)
-    e = launch_combine(y, inv, w, T, k, H, static_cast<__nv_bfloat16*>(out_bf16), o);
-  if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, msg_of("kernel launch", e));
-  return RIMURU_OK;
+  LayerLaunch a;
+  a.x = x_bf16;
+  a.logits = logits;
+  a.out = out_bf16;
+  a.T = T;
+  a.E = E;
+  a.k = k;
+  a.H = H;
+  a.I = I;
+  a.renorm = v.renorm;
+  a.num_pages = static_cast<int>(v.n_pages);
+  a.ws = ws;
+  a.layout = L;
+  a.table = table;
+  a.err = err;
+  a.tm_w13 = &tm_w13;
+  a.tm_w2 = &tm_w2;
+  a.stream = stream;
+  a.sm_count = sms;
+  return launch_layer(a);
 }

@@ -246,8 +246,12 @@ def rimuru_kernel_name(k: int):
     return n.decode() if n else None
 
 
-def rimuru_profile_enable(view, enable: bool, capacity: int = 1024) -> None:
-    _check(lib.rimuru_profile_enable(view, int(enable), capacity))
+PROFILE_ALL = (1 << K_COUNT) - 1
+
+
+def rimuru_profile_enable(view, kernel_mask: int, capacity: int = 1024) -> None:
+    """Bracket the kernels in ``kernel_mask`` (bit K_*) with CUDA events; 0 stops."""
+    _check(lib.rimuru_profile_enable(view, int(kernel_mask), capacity))
 
 
 def rimuru_profile_read(view, k: int):
