@@ -41,7 +41,12 @@ constexpr int kBBytes = 4 * kBChunk;         // 32 KiB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 2 * BN;            // two accumulators
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align slack*/ + 256 /*barriers*/;
+// Epilogue staging: per epilogue warp one 32-row x 64-column bf16 block (4 KiB),
+// 128-byte rows with 16-byte chunks XOR-swizzled by row so that both the
+// row-per-lane writes and the row-segment reads are free of bank conflicts.
+constexpr int kStageOutBytes = 32 * 128;
+constexpr int kSmemBytes = kStages * kStageBytes + 4 * kStageOutBytes + 1024 /*align slack*/ +
+                           256 /*barriers*/;
 
 struct Shared {
   uint64_t full[kStages];
@@ -62,7 +67,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  Shared* sh = reinterpret_cast<Shared*>(smem + kStages * kStageBytes);
+  uint8_t* sOut = smem + kStages * kStageBytes;  // 4 epilogue blocks
+  Shared* sh = reinterpret_cast<Shared*>(sOut + 4 * kStageOutBytes);
   volatile int* abort = &sh->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -198,7 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may read
-    const int r = q * 32 + lane;
     uint32_t local = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
       const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
@@ -214,10 +219,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
       const int e = p.tiles[2 * mb], row0 = p.tiles[2 * mb + 1];
       const int rows = min(BM, p.offsets[e + 1] - row0);
-      const bool valid = r < rows;
-      __nv_bfloat16* orow = p.out + static_cast<size_t>(row0 + r) * p.ldo;
       const uint32_t tb = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (kSwiGLU) {
+        // GEMM 1: each lane writes its own row of h, 32 columns at a time.
+        const int r = q * 32 + lane;
+        const bool valid = r < rows;
+        __nv_bfloat16* orow = p.out + static_cast<size_t>(row0 + r) * p.ldo;
         const int n0 = nb * (BN / 2);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN / 2; c0 += 32) {
@@ -229,37 +236,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c0);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              o.x = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 0]), __uint_as_float(u[8 * v + 0])),
-                                silu_mul(__uint_as_float(g[8 * v + 1]), __uint_as_float(u[8 * v + 1])));
-              o.y = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 2]), __uint_as_float(u[8 * v + 2])),
-                                silu_mul(__uint_as_float(g[8 * v + 3]), __uint_as_float(u[8 * v + 3])));
-              o.z = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 4]), __uint_as_float(u[8 * v + 4])),
-                                silu_mul(__uint_as_float(g[8 * v + 5]), __uint_as_float(u[8 * v + 5])));
-              o.w = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 6]), __uint_as_float(u[8 * v + 6])),
-                                silu_mul(__uint_as_float(g[8 * v + 7]), __uint_as_float(u[8 * v + 7])));
-              dst[v] = o;
+              uint32_t o[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int c = 8 * v + 2 * i;
+                o[i] = pack_bf16x2(silu_mul(__uint_as_float(g[c]), __uint_as_float(u[c])),
+                                   silu_mul(__uint_as_float(g[c + 1]), __uint_as_float(u[c + 1])));
+              }
+              dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
             }
           }
         }
       } else {
+        // GEMM 2: rows q*32 .. q*32+31 go out in blocks of 64 columns; each
+        // lane packs its own row into the staging block, then each store
+        // instruction writes four complete 128-byte row segments.
+        const uint32_t blk_s = smem_u32(sOut + q * kStageOutBytes);
         const int n0 = nb * BN;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          uint32_t a[32];
-          tmem_ld32(tb + c0, a);
-          tmem_ld_wait();
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c0);
+        for (int c0 = 0; c0 < BN; c0 += 64) {
+          uint32_t packed[32];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(a[8 * v + 0]), __uint_as_float(a[8 * v + 1]));
-              o.y = pack_bf16x2(__uint_as_float(a[8 * v + 2]), __uint_as_float(a[8 * v + 3]));
-              o.z = pack_bf16x2(__uint_as_float(a[8 * v + 4]), __uint_as_float(a[8 * v + 5]));
-              o.w = pack_bf16x2(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7]));
-              dst[v] = o;
-            }
+          for (int half = 0; half < 2; ++half) {
+            uint32_t a[32];
+            tmem_ld32(tb + c0 + 32 * half, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              packed[16 * half + i] =
+                  pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+          }
+          __syncwarp();  // the previous block has been read out
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t at = blk_s + lane * 128 + ((c ^ (lane & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(at), "r"(packed[4 * c]),
+                         "r"(packed[4 * c + 1]), "r"(packed[4 * c + 2]), "r"(packed[4 * c + 3])
+                         : "memory");
+          }
+          __syncwarp();
+          const int chunk = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3);  // row within this warp's 32
+            uint4 v;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(blk_s + rr * 128 + ((chunk ^ (rr & 7)) << 4))
+                         : "memory");
+            if (q * 32 + rr < rows)
+              *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(row0 + q * 32 + rr) * p.ldo +
+                                        n0 + c0 + chunk * 8) = v;
           }
         }
       }

@@ -233,16 +233,28 @@ __global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
 }
 
 // ----------------------------------------------------------------- gather
+// Each CTA copies kGatherRows rows per iteration, with every load issued
+// before the first store so several 16-byte loads per thread are in flight.
+constexpr int kGatherRows = 4;
+
 __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict__ x,
                                                          const int32_t* __restrict__ sorted, int A,
                                                          int k, int H8, uint4* __restrict__ xs) {
   grid_dep_wait();
   grid_dep_launch();
-  for (int r = blockIdx.x; r < A; r += gridDim.x) {
-    const int t = sorted[r] / k;
-    const uint4* src = x + static_cast<size_t>(t) * H8;
-    uint4* dst = xs + static_cast<size_t>(r) * H8;
-    for (int c = threadIdx.x; c < H8; c += blockDim.x) dst[c] = src[c];
+  for (int r0 = blockIdx.x * kGatherRows; r0 < A; r0 += gridDim.x * kGatherRows) {
+    int t[kGatherRows];
+#pragma unroll
+    for (int i = 0; i < kGatherRows; ++i) t[i] = (r0 + i < A) ? sorted[r0 + i] / k : -1;
+    for (int c = threadIdx.x; c < H8; c += blockDim.x) {
+      uint4 v[kGatherRows];
+#pragma unroll
+      for (int i = 0; i < kGatherRows; ++i)
+        if (t[i] >= 0) v[i] = x[static_cast<size_t>(t[i]) * H8 + c];
+#pragma unroll
+      for (int i = 0; i < kGatherRows; ++i)
+        if (t[i] >= 0) xs[static_cast<size_t>(r0 + i) * H8 + c] = v[i];
+    }
   }
 }
 
@@ -326,7 +338,8 @@ cudaError_t launch_align(const int32_t* ids, const int32_t* chunk_hist, int chun
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted, int A, int k, int H,
                           __nv_bfloat16* x_sorted, const LaunchOpts& o) {
-  const int grid = min(A, o.sm_count * 8);
+  const int blocks = (A + kGatherRows - 1) / kGatherRows;
+  const int grid = min(blocks, o.sm_count * 8);
   return launch(moe_gather_kernel, dim3(grid), dim3(256), 0, o, reinterpret_cast<const uint4*>(x),
                 sorted, A, k, H / 8, reinterpret_cast<uint4*>(x_sorted));
 }
