@@ -339,6 +339,16 @@ int rimuru_profile_read(rimuru_view_t view, int k, int* launches, double* total_
  * device is visible). */
 int rimuru_device_sm_count(void);
 
+/* Failure-path self-test (no counterpart in the pages; it checks this
+ * library's own safety net).  Launches one kernel on the current device
+ * whose threads wait on an mbarrier that nothing ever arrives on, using the
+ * same bounded wait as every pipeline stage of the GEMM kernels, with a limit
+ * of `timeout_us` microseconds (at most 2 s).  The kernel gives up, records
+ * RIMURU_DEV_TIMEOUT in a device status word and returns; the call
+ * synchronises the device and stores that word in *status_out (expected:
+ * RIMURU_DEV_TIMEOUT).  Nothing traps and the context stays usable. */
+int rimuru_selftest_bounded_wait(uint32_t timeout_us, int* status_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -39,7 +39,7 @@ EXPORTS = [
     "rimuru_moe_workspace_bytes", "rimuru_moe_workspace_layout", "rimuru_moe_forward",
     "rimuru_moe_forward_noalloc",
     "rimuru_get_device_error", "rimuru_kernel_name", "rimuru_profile_enable",
-    "rimuru_profile_read", "rimuru_device_sm_count",
+    "rimuru_profile_read", "rimuru_device_sm_count", "rimuru_selftest_bounded_wait",
 ]
 
 
@@ -94,6 +94,7 @@ def _load():
         "rimuru_profile_enable": ([P, i32, i32], i32),
         "rimuru_profile_read": ([P, i32, ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_double)], i32),
         "rimuru_device_sm_count": ([], i32),
+        "rimuru_selftest_bounded_wait": ([ctypes.c_uint32, ctypes.POINTER(i32)], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -262,3 +263,10 @@ def rimuru_profile_read(view, k: int):
 
 def rimuru_device_sm_count() -> int:
     return int(lib.rimuru_device_sm_count())
+
+
+def rimuru_selftest_bounded_wait(timeout_us: int) -> int:
+    """Run the bounded-wait self-test kernel; returns the device status it recorded."""
+    st = ctypes.c_int()
+    _check(lib.rimuru_selftest_bounded_wait(int(timeout_us), ctypes.byref(st)))
+    return st.value

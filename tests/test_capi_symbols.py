@@ -33,3 +33,12 @@ def test_status_strings():
     assert R.rimuru_status_string(-4) == "RIMURU_ERR_UNMAPPED"
     assert R.rimuru_kernel_name(R.K_GEMM1) == "moe_gemm1_swiglu"
     assert R.rimuru_kernel_name(99) is None
+
+
+def test_selftest_rejects_bad_limits_before_touching_a_device():
+    import pytest
+    from paged_moe_shared_gb300 import rimuru as R
+    for bad in (0, 3_000_000):
+        with pytest.raises(R.RimuruError) as e:
+            R.rimuru_selftest_bounded_wait(bad)
+        assert e.value.status == R.ERR_ARG
