@@ -302,6 +302,70 @@ int rimuru_moe_forward_noalloc(const void* x_bf16, const float* logits, int num_
                                rimuru_view_t view, int layer, void* out_bf16, int* dev_error,
                                void* stream);
 
+/* ------------------------------------------------------ expert offloading */
+
+/*
+ * Expert offloading for a stack of layers (Rimuru page, Figure 1 panel b and
+ * the explainer's motivation paragraph: experts kept in CPU memory with a
+ * device cache of resident experts; Figure 8: two buffers so that expert
+ * prefetch overlaps execution without a device-to-device copy).  Every
+ * expert of every layer lives in pinned host memory; `capacity_experts` of
+ * them are resident at a time, each in three pages of the expert view that
+ * the cache allocates at creation.  A miss is copied host -> device on the
+ * copy stream straight into the pages of the least recently used slot
+ * (this library's choice: the pages name no eviction policy).
+ *
+ * host_pages  pinned host memory (cudaHostAlloc or registered) holding
+ *             layers * experts * 3 pages of the view's page size; projection
+ *             p of expert e in layer l starts at page (l * experts + e) * 3 +
+ *             p, bf16 row-major as for rimuru_expert_map.  Must outlive the
+ *             cache and stay unchanged.
+ * capacity_experts  resident experts (1 .. layers * experts); the pool must
+ *             have 3 * capacity free pages of the view's size.
+ * copy_stream stream for the host -> device copies (NULL: the cache creates
+ *             one).
+ * The view's page table must be empty: the cache maps and unmaps entries as
+ * experts come and go.  Ordering is kept on the GPU: a slot is overwritten
+ * only after the last forward that read it has finished, and a forward reads
+ * a layer's slots only after their copies have landed.
+ */
+typedef struct rimuru_offload_s* rimuru_offload_t;
+
+typedef struct rimuru_offload_counters {
+  int64_t forwards;        /* rimuru_offload_forward calls */
+  int64_t hits;            /* routed experts already resident when routing finished */
+  int64_t misses;          /* routed experts copied in on demand */
+  int64_t prefetch_loads;  /* experts copied in by rimuru_offload_prefetch */
+  int64_t evictions;       /* resident experts replaced */
+  int64_t bytes_h2d;       /* bytes copied host -> device */
+} rimuru_offload_counters;
+
+int rimuru_offload_create(rimuru_view_t view, const void* host_pages, int capacity_experts,
+                          void* copy_stream, rimuru_offload_t* out);
+/* Waits for the copy stream, unmaps and frees every slot page. */
+int rimuru_offload_destroy(rimuru_offload_t off);
+
+/* Queue copies on the copy stream that make the listed experts (host array
+ * of n expert ids) of `layer` resident, evicting least recently used ones.
+ * Returns at once; call it for layer l + 1 before the forward of layer l so
+ * the copies overlap that layer's kernels. */
+int rimuru_offload_prefetch(rimuru_offload_t off, int layer, const int32_t* experts, int n);
+
+/* The fused MoE layer of rimuru_moe_forward for `layer`, with experts brought
+ * in as needed: routing runs first, the host reads the per-expert counts
+ * back (this call waits for the routing kernels), every routed expert that
+ * is not resident is copied in, the layer's page-table slice is uploaded,
+ * and the expert kernels run once the copies they need have landed.
+ * Arguments and errors as rimuru_moe_forward; RIMURU_ERR_OOM if one layer
+ * routes to more experts than the capacity. */
+int rimuru_offload_forward(rimuru_offload_t off, const void* x_bf16, const float* logits,
+                           int num_tokens, int layer, void* out_bf16, void* workspace,
+                           uint64_t workspace_bytes, void* stream);
+
+int rimuru_offload_stats(rimuru_offload_t off, rimuru_offload_counters* out);
+/* Slot holding (layer, expert), or -1 when it is not resident. */
+int rimuru_offload_resident(rimuru_offload_t off, int layer, int expert, int* slot);
+
 /* Device error word of the view (RIMURU_DEV_*).  Synchronises with the
  * device (cudaMemcpy) so call it after the forward's stream has been
  * synchronised; clear != 0 resets it to RIMURU_DEV_OK. */

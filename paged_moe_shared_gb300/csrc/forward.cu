@@ -77,6 +77,8 @@ void layout_for(const View& v, int T, rimuru_ws_layout* L) {
   L->max_tiles = static_cast<int32_t>(max_tiles);
 }
 
+}  // namespace
+
 int ensure_device_state(View* v) {
   if (v->dev) return RIMURU_OK;
   auto* d = new (std::nothrow) DeviceState;
@@ -105,6 +107,20 @@ int ensure_device_state(View* v) {
   v->table_dirty = true;
   return RIMURU_OK;
 }
+
+int view_device_table(View* v, int32_t** table, int** err, const CUtensorMap** w13,
+                      const CUtensorMap** w2, int* device) {
+  int st = ensure_device_state(v);
+  if (st != RIMURU_OK) return st;
+  *table = v->dev->d_table;
+  *err = v->dev->d_err;
+  *w13 = &v->dev->tm_w13;
+  *w2 = &v->dev->tm_w2;
+  *device = v->dev->device;
+  return RIMURU_OK;
+}
+
+namespace {
 
 int upload_table(View* v, cudaStream_t stream) {
   DeviceState* d = v->dev;

@@ -99,5 +99,10 @@ struct LayerLaunch {
 
 // Launch the six kernels of one layer.  Returns a rimuru status.
 int launch_layer(const LayerLaunch& a);
+// The same in two halves: routing (route, align) and the expert part (gather,
+// GEMM 1, GEMM 2, combine).  Host-side work may sit between the two;
+// after_route = false when it does (the gather then follows it in stream order).
+int launch_layer_route(const LayerLaunch& a);
+int launch_layer_experts(const LayerLaunch& a, bool after_route);
 
 }  // namespace rimuru

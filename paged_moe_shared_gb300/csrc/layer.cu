@@ -68,98 +68,133 @@ int make_weight_maps(void* pool_base, uint64_t page_bytes, int64_t n_pages, int 
   return st;
 }
 
-int launch_layer(const LayerLaunch& a) {
+namespace {
+
+struct LayerPtrs {
+  int32_t *ids, *chunk_hist, *offsets, *sorted, *inv, *tiles, *num_tiles;
+  float* w;
+  __nv_bfloat16 *xs, *h, *y;
+};
+
+LayerPtrs pointers_of(const LayerLaunch& a) {
   const rimuru_ws_layout& L = a.layout;
-  const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I;
-  const int A = T * k;
   uint8_t* ws = a.ws;
-  auto* ids = reinterpret_cast<int32_t*>(ws + L.ids);
-  auto* w = reinterpret_cast<float*>(ws + L.weights);
-  auto* chunk_hist = reinterpret_cast<int32_t*>(ws + L.chunk_hist);
-  auto* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
-  auto* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
-  auto* inv = reinterpret_cast<int32_t*>(ws + L.inv);
-  auto* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
-  auto* num_tiles = reinterpret_cast<int32_t*>(ws + L.num_tiles);
-  auto* xs = reinterpret_cast<__nv_bfloat16*>(ws + L.x_sorted);
-  auto* h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
-  auto* y = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
+  LayerPtrs q;
+  q.ids = reinterpret_cast<int32_t*>(ws + L.ids);
+  q.w = reinterpret_cast<float*>(ws + L.weights);
+  q.chunk_hist = reinterpret_cast<int32_t*>(ws + L.chunk_hist);
+  q.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  q.sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
+  q.inv = reinterpret_cast<int32_t*>(ws + L.inv);
+  q.tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
+  q.num_tiles = reinterpret_cast<int32_t*>(ws + L.num_tiles);
+  q.xs = reinterpret_cast<__nv_bfloat16*>(ws + L.x_sorted);
+  q.h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
+  q.y = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
+  return q;
+}
 
-  // activation maps: x_sorted [A][H] and h [A][I], 64 x 128 boxes
-  CUtensorMap tm_x, tm_h;
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(A)};
-    cuuint64_t str[1] = {static_cast<cuuint64_t>(H) * 2};
-    cuuint32_t box[2] = {64, 128};
-    int st = make_bf16_map(&tm_x, xs, 2, dims, str, box);
-    if (st != RIMURU_OK) return st;
-  }
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(I), static_cast<cuuint64_t>(A)};
-    cuuint64_t str[1] = {static_cast<cuuint64_t>(I) * 2};
-    cuuint32_t box[2] = {64, 128};
-    int st = make_bf16_map(&tm_h, h, 2, dims, str, box);
-    if (st != RIMURU_OK) return st;
-  }
+}  // namespace
 
-  GemmArgs g1{};
-  g1.page_table = a.table;
-  g1.tiles = tiles;
-  g1.num_tiles = num_tiles;
-  g1.offsets = offsets;
-  g1.num_pages = a.num_pages;
-  g1.max_tiles = L.max_tiles;
-  g1.weights_evict_first = (A <= E * kTileM / 4) ? 1 : 0;
-  g1.err = a.err;
-  GemmArgs g2 = g1;
-  g1.out = h;
-  g1.ldo = I;
-  g1.n_blocks = I / 128;
-  g1.num_k_blocks = H / 64;
-  g2.out = y;
-  g2.ldo = H;
-  g2.n_blocks = H / 256;
-  g2.num_k_blocks = I / 64;
-
+int launch_layer_route(const LayerLaunch& a) {
+  const LayerPtrs q = pointers_of(a);
   LaunchOpts first;
   first.stream = a.stream;
   first.sm_count = a.sm_count;
   first.pdl = false;  // the first kernel follows whatever the caller queued
   LaunchOpts next = first;
   next.pdl = a.pdl;
-
   cudaError_t e = cudaSuccess;
   auto mark = [&](int kidx, int which) {
     if (a.ev && (a.ev_mask >> kidx & 1u) && e == cudaSuccess)
       e = cudaEventRecord(a.ev[kidx * 2 + which], a.stream);
   };
-  const int tpc = tokens_per_chunk(k);
-
+  const int tpc = tokens_per_chunk(a.k);
   mark(RIMURU_K_ROUTE, 0);
   if (e == cudaSuccess)
-    e = launch_route(a.logits, T, E, k, a.renorm, tpc, ids, w, chunk_hist, a.err, first);
+    e = launch_route(a.logits, a.T, a.E, a.k, a.renorm, tpc, q.ids, q.w, q.chunk_hist, a.err, first);
   mark(RIMURU_K_ROUTE, 1);
   mark(RIMURU_K_ALIGN, 0);
   if (e == cudaSuccess)
-    e = launch_align(ids, chunk_hist, L.chunks, A, E, tpc * k, offsets, sorted, inv, tiles,
-                     num_tiles, a.err, next);
+    e = launch_align(q.ids, q.chunk_hist, a.layout.chunks, a.T * a.k, a.E, tpc * a.k, q.offsets,
+                     q.sorted, q.inv, q.tiles, q.num_tiles, a.err, next);
   mark(RIMURU_K_ALIGN, 1);
+  if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, cuda_msg("kernel launch", e));
+  return RIMURU_OK;
+}
+
+int launch_layer_experts(const LayerLaunch& a, bool after_route) {
+  const rimuru_ws_layout& L = a.layout;
+  const LayerPtrs q = pointers_of(a);
+  const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I;
+  const int A = T * k;
+  CUtensorMap tm_x, tm_h;
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(A)};
+    cuuint64_t str[1] = {static_cast<cuuint64_t>(H) * 2};
+    cuuint32_t box[2] = {64, 128};
+    int st = make_bf16_map(&tm_x, q.xs, 2, dims, str, box);
+    if (st != RIMURU_OK) return st;
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(I), static_cast<cuuint64_t>(A)};
+    cuuint64_t str[1] = {static_cast<cuuint64_t>(I) * 2};
+    cuuint32_t box[2] = {64, 128};
+    int st = make_bf16_map(&tm_h, q.h, 2, dims, str, box);
+    if (st != RIMURU_OK) return st;
+  }
+  GemmArgs g1{};
+  g1.page_table = a.table;
+  g1.tiles = q.tiles;
+  g1.num_tiles = q.num_tiles;
+  g1.offsets = q.offsets;
+  g1.num_pages = a.num_pages;
+  g1.max_tiles = L.max_tiles;
+  g1.weights_evict_first = (A <= E * kTileM / 4) ? 1 : 0;
+  g1.err = a.err;
+  GemmArgs g2 = g1;
+  g1.out = q.h;
+  g1.ldo = I;
+  g1.n_blocks = I / 128;
+  g1.num_k_blocks = H / 64;
+  g2.out = q.y;
+  g2.ldo = H;
+  g2.n_blocks = H / 256;
+  g2.num_k_blocks = I / 64;
+
+  LaunchOpts o;
+  o.stream = a.stream;
+  o.sm_count = a.sm_count;
+  o.pdl = a.pdl;
+  LaunchOpts gather_o = o;
+  gather_o.pdl = after_route && a.pdl;  // directly behind align, or behind host-side work
+  cudaError_t e = cudaSuccess;
+  auto mark = [&](int kidx, int which) {
+    if (a.ev && (a.ev_mask >> kidx & 1u) && e == cudaSuccess)
+      e = cudaEventRecord(a.ev[kidx * 2 + which], a.stream);
+  };
   mark(RIMURU_K_GATHER, 0);
   if (e == cudaSuccess)
-    e = launch_gather(static_cast<const __nv_bfloat16*>(a.x), sorted, A, k, H, xs, next);
+    e = launch_gather(static_cast<const __nv_bfloat16*>(a.x), q.sorted, A, k, H, q.xs, gather_o);
   mark(RIMURU_K_GATHER, 1);
   mark(RIMURU_K_GEMM1, 0);
-  if (e == cudaSuccess) e = launch_gemm1_swiglu(tm_x, *a.tm_w13, g1, next);
+  if (e == cudaSuccess) e = launch_gemm1_swiglu(tm_x, *a.tm_w13, g1, o);
   mark(RIMURU_K_GEMM1, 1);
   mark(RIMURU_K_GEMM2, 0);
-  if (e == cudaSuccess) e = launch_gemm2(tm_h, *a.tm_w2, g2, next);
+  if (e == cudaSuccess) e = launch_gemm2(tm_h, *a.tm_w2, g2, o);
   mark(RIMURU_K_GEMM2, 1);
   mark(RIMURU_K_COMBINE, 0);
   if (e == cudaSuccess)
-    e = launch_combine(y, inv, w, T, k, H, static_cast<__nv_bfloat16*>(a.out), next);
+    e = launch_combine(q.y, q.inv, q.w, T, k, H, static_cast<__nv_bfloat16*>(a.out), o);
   mark(RIMURU_K_COMBINE, 1);
   if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, cuda_msg("kernel launch", e));
   return RIMURU_OK;
+}
+
+int launch_layer(const LayerLaunch& a) {
+  int st = launch_layer_route(a);
+  if (st != RIMURU_OK) return st;
+  return launch_layer_experts(a, /*after_route=*/true);
 }
 
 }  // namespace rimuru

@@ -40,6 +40,8 @@ EXPORTS = [
     "rimuru_moe_forward_noalloc",
     "rimuru_get_device_error", "rimuru_kernel_name", "rimuru_profile_enable",
     "rimuru_profile_read", "rimuru_device_sm_count", "rimuru_selftest_bounded_wait",
+    "rimuru_offload_create", "rimuru_offload_destroy", "rimuru_offload_prefetch",
+    "rimuru_offload_forward", "rimuru_offload_stats", "rimuru_offload_resident",
 ]
 
 
@@ -59,6 +61,11 @@ class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "ids", "weights", "chunk_hist", "offsets", "sorted", "inv", "tiles", "num_tiles",
         "x_sorted", "h", "y", "total")] + [("chunks", ctypes.c_int32), ("max_tiles", ctypes.c_int32)]
+
+
+class OffloadCounters(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "forwards", "hits", "misses", "prefetch_loads", "evictions", "bytes_h2d")]
 
 
 def _load():
@@ -95,6 +102,12 @@ def _load():
         "rimuru_profile_read": ([P, i32, ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_double)], i32),
         "rimuru_device_sm_count": ([], i32),
         "rimuru_selftest_bounded_wait": ([ctypes.c_uint32, ctypes.POINTER(i32)], i32),
+        "rimuru_offload_create": ([P, P, i32, P, ctypes.POINTER(P)], i32),
+        "rimuru_offload_destroy": ([P], i32),
+        "rimuru_offload_prefetch": ([P, i32, P, i32], i32),
+        "rimuru_offload_forward": ([P, P, P, i32, i32, P, P, u64, P], i32),
+        "rimuru_offload_stats": ([P, ctypes.POINTER(OffloadCounters)], i32),
+        "rimuru_offload_resident": ([P, i32, i32, ctypes.POINTER(i32)], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -270,3 +283,40 @@ def rimuru_selftest_bounded_wait(timeout_us: int) -> int:
     st = ctypes.c_int()
     _check(lib.rimuru_selftest_bounded_wait(int(timeout_us), ctypes.byref(st)))
     return st.value
+
+
+def rimuru_offload_create(view, host_pages_ptr: int, capacity_experts: int, copy_stream: int = 0):
+    h = ctypes.c_void_p()
+    _check(lib.rimuru_offload_create(view, ctypes.c_void_p(host_pages_ptr), capacity_experts,
+                                     ctypes.c_void_p(copy_stream or None), ctypes.byref(h)))
+    return h
+
+
+def rimuru_offload_destroy(off) -> None:
+    _check(lib.rimuru_offload_destroy(off))
+
+
+def rimuru_offload_prefetch(off, layer: int, experts) -> None:
+    arr = (ctypes.c_int32 * len(experts))(*[int(e) for e in experts])
+    _check(lib.rimuru_offload_prefetch(off, layer, ctypes.cast(arr, ctypes.c_void_p), len(experts)))
+
+
+def rimuru_offload_forward(off, x_ptr: int, logits_ptr: int, num_tokens: int, layer: int,
+                           out_ptr: int, workspace_ptr: int, workspace_bytes: int,
+                           stream: int = 0) -> None:
+    _check(lib.rimuru_offload_forward(off, ctypes.c_void_p(x_ptr), ctypes.c_void_p(logits_ptr),
+                                      num_tokens, layer, ctypes.c_void_p(out_ptr),
+                                      ctypes.c_void_p(workspace_ptr), workspace_bytes,
+                                      ctypes.c_void_p(stream)))
+
+
+def rimuru_offload_stats(off) -> dict:
+    c = OffloadCounters()
+    _check(lib.rimuru_offload_stats(off, ctypes.byref(c)))
+    return {f: getattr(c, f) for f, _ in OffloadCounters._fields_}
+
+
+def rimuru_offload_resident(off, layer: int, expert: int) -> int:
+    s = ctypes.c_int()
+    _check(lib.rimuru_offload_resident(off, layer, expert, ctypes.byref(s)))
+    return s.value

@@ -1,0 +1,146 @@
+"""Expert offloading: every layer's output against the oracle, and the cache's hit, miss,
+prefetch and eviction counts against an independent model of the policy (least recently
+used slot first; slots claimed by the same prefetch or forward are never evicted by it).
+
+Rimuru page: experts kept in CPU memory with a device cache (Figure 1 panel b) and dual
+buffers that overlap prefetch with execution (Figure 8)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from gpu_harness import bf16_tensor, rel_err, to_f64
+from oracle import Oracle
+from paged_moe_shared_gb300 import rimuru as R
+from paged_moe_shared_gb300.device_pool import DevicePool
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+class LRUModel:
+    """Slots in recency order (index 0 = most recent); initially slot 0 is the oldest."""
+
+    def __init__(self, cap):
+        self.order = list(range(cap - 1, -1, -1))
+        self.slot_key = [None] * cap
+        self.key_slot = {}
+        self.claimed = {}
+        self.op = 0
+        self.c = dict(hits=0, misses=0, prefetch_loads=0, evictions=0, bytes_h2d=0, forwards=0)
+
+    def _load(self, key, demand, nbytes):
+        s = self.key_slot.get(key)
+        if s is not None:
+            self.order.remove(s)
+            self.order.insert(0, s)
+            self.claimed[s] = self.op
+            return True
+        for s in reversed(self.order):
+            if self.claimed.get(s) != self.op:
+                break
+        else:
+            raise AssertionError("capacity too small")
+        old = self.slot_key[s]
+        if old is not None:
+            del self.key_slot[old]
+            self.c["evictions"] += 1
+        self.slot_key[s] = key
+        self.key_slot[key] = s
+        self.claimed[s] = self.op
+        self.order.remove(s)
+        self.order.insert(0, s)
+        self.c["bytes_h2d"] += nbytes
+        if not demand:
+            self.c["prefetch_loads"] += 1
+        return False
+
+    def prefetch(self, keys, nbytes):
+        self.op += 1
+        for k in keys:
+            self._load(k, False, nbytes)
+
+    def forward(self, keys, nbytes):
+        self.op += 1
+        for k in keys:
+            hit = self._load(k, True, nbytes)
+            self.c["hits" if hit else "misses"] += 1
+        self.c["forwards"] += 1
+
+
+def run_stack(st: wl.OffloadStack, cap: int, prefetch: bool):
+    s = st.shape
+    E = s.E
+    pb = st.page_bytes
+    oracle = Oracle()
+    host = torch.from_numpy(st.host_pages).pin_memory()
+    pool = DevicePool((3 * cap + 5) * pb, pb, DEV)
+    ev = pool.view(pb)
+    R.rimuru_view_set_moe_shape(ev, st.L, E, s.H, s.I, s.k, s.renorm)
+    pool.upload(wl.empty_pool((3 * cap + 5) * pb))
+    off = R.rimuru_offload_create(ev, host.data_ptr(), cap, 0)
+    model = LRUModel(cap)
+    nbytes = 3 * s.H * s.I * 2
+    ws_bytes = R.rimuru_moe_workspace_bytes(ev, st.T)
+    ws_raw = torch.empty(ws_bytes + 1024, dtype=torch.uint8, device=DEV)
+    ws_ptr = (ws_raw.data_ptr() + 1023) // 1024 * 1024
+    stream = torch.cuda.current_stream().cuda_stream
+    prev_routed = {}
+    worst = 0.0
+    try:
+        for step in range(st.steps):
+            for l in range(st.L):
+                o = oracle.moe_forward(st.x_bits[step][l], st.logits[step][l], st.host_pages, pb,
+                                       st.layer_table(l), s.H, s.I, s.k, s.renorm)
+                routed = sorted(set(o["ids"].ravel().tolist()))
+                if prefetch and l + 1 < st.L and (l + 1) in prev_routed:
+                    guess = prev_routed[l + 1]
+                    R.rimuru_offload_prefetch(off, l + 1, guess)
+                    model.prefetch([(l + 1) * E + e for e in guess], nbytes)
+                x = bf16_tensor(st.x_bits[step][l])
+                lg = torch.from_numpy(st.logits[step][l]).to(DEV)
+                out = torch.empty_like(x)
+                R.rimuru_offload_forward(off, x.data_ptr(), lg.data_ptr(), st.T, l, out.data_ptr(),
+                                         ws_ptr, ws_bytes, stream)
+                model.forward([l * E + e for e in routed], nbytes)
+                torch.cuda.synchronize()
+                assert R.rimuru_get_device_error(ev, clear=True) == R.DEV_OK
+                err = rel_err(to_f64(out), o["out"])
+                assert err <= 1e-2, (step, l, err)
+                worst = max(worst, err)
+                prev_routed[l] = routed
+                for e in range(E):  # residency matches the model
+                    assert (R.rimuru_offload_resident(off, l, e) >= 0) == ((l * E + e) in model.key_slot)
+        counters = R.rimuru_offload_stats(off)
+    finally:
+        R.rimuru_offload_destroy(off)
+        pool.close()
+    return counters, model.c, worst
+
+
+@pytest.mark.parametrize("prefetch,cap", [(False, 12), (True, 12), (True, 20)],
+                         ids=["demand_only_12", "prefetch_12", "prefetch_20"])
+def test_offloaded_stack_matches_oracle_and_lru_model(prefetch, cap):
+    """6 tiny layers (8 experts, top-2), 16 tokens, 3 steps; 12 or 20 of 48 experts resident.
+    With 12 slots (less than two layers' worth) prefetching layer l + 1 evicts what was
+    prefetched for layer l, so only 20 slots let prefetched experts be hit."""
+    shape = wl.MoEShape(H=256, I=128, E=8, k=2)
+    st = wl.offload_stack(shape, L=6, T=16, steps=3, seed=51)
+    counters, expected, worst = run_stack(st, cap=cap, prefetch=prefetch)
+    assert counters == expected
+    assert counters["misses"] + counters["prefetch_loads"] > 0 and counters["evictions"] > 0
+    if prefetch:
+        assert counters["prefetch_loads"] > 0
+    if cap == 20:
+        assert counters["hits"] > 0
+
+
+def test_capacity_below_one_layer_is_rejected():
+    """Every token routes to 2 of 8 experts, so 16 tokens touch more than 3 experts."""
+    shape = wl.MoEShape(H=256, I=128, E=8, k=2)
+    st = wl.offload_stack(shape, L=2, T=16, steps=1, seed=52)
+    with pytest.raises(R.RimuruError) as e:
+        run_stack(st, cap=3, prefetch=False)
+    assert e.value.status == R.ERR_OOM

@@ -207,6 +207,55 @@ def build_mixed(shape: MoEShape, T: int, seed: int, kv_huge_pages: int | None = 
                            "free_huge_pages": free_huge_pages, "seed": seed})
 
 
+@dataclass
+class OffloadStack:
+    """Host image of every expert page of an L-layer stack plus per-(step, layer) inputs.
+    Projection p of expert e in layer l is host page (l * E + e) * 3 + p."""
+    shape: MoEShape
+    L: int
+    T: int
+    steps: int
+    page_bytes: int
+    host_pages: np.ndarray        # uint8 [L * E * 3 * page_bytes]
+    x_bits: list                  # [steps][L] uint16 [T, H]
+    logits: list                  # [steps][L] float32 [T, E]
+
+    def layer_table(self, layer: int) -> np.ndarray:
+        E = self.shape.E
+        return (np.arange(E * 3, dtype=np.int32) + layer * E * 3).reshape(E, 3)
+
+
+def offload_stack(shape: MoEShape, L: int, T: int, steps: int, seed: int,
+                  distinct_layers: int | None = None, host: np.ndarray | None = None,
+                  distinct_inputs: int | None = None) -> OffloadStack:
+    """Seeded stack.  With ``distinct_layers = d``, layer l copies the values of layer l % d
+    with the lowest mantissa bit flipped when (l // d) is odd (cheap to make for 48 layers of
+    Qwen3 size); None gives every layer its own draws.  ``host`` may be a caller buffer
+    (e.g. pinned) of the right size.  With ``distinct_inputs = n`` only n (x, logits) pairs
+    are drawn and (step, layer) uses pair (step * L + layer) % n."""
+    H, I, E = shape.H, shape.I, shape.E
+    pb = H * I * 2
+    if host is None:
+        host = np.empty(L * E * 3 * pb, np.uint8)
+    assert host.dtype == np.uint8 and host.size == L * E * 3 * pb
+    words = host.view(np.uint16).reshape(L, E, 3, H * I)
+    d = L if distinct_layers is None else distinct_layers
+    for l in range(L):
+        if l < d:
+            w1, w3, w2 = make_expert_weights(seed * 1000 + l, shape)
+            words[l, :, 0] = w1.reshape(E, -1)
+            words[l, :, 1] = w3.reshape(E, -1)
+            words[l, :, 2] = w2.reshape(E, -1)
+        else:
+            np.bitwise_xor(words[l % d], np.uint16(l // d & 1), out=words[l])
+    n = steps * L if distinct_inputs is None else distinct_inputs
+    px = [make_x(seed * 7919 + i, T, H) for i in range(n)]
+    pl = [make_logits(seed * 7919 + i, px[i], E) for i in range(n)]
+    xs = [[px[(s * L + l) % n] for l in range(L)] for s in range(steps)]
+    lg = [[pl[(s * L + l) % n] for l in range(L)] for s in range(steps)]
+    return OffloadStack(shape, L, T, steps, pb, host, xs, lg)
+
+
 # Named configurations -------------------------------------------------------------
 
 TINY = MoEShape(H=256, I=128, E=8, k=2)
