@@ -171,6 +171,25 @@ int rimuru_page_alloc(rimuru_view_t view, int64_t* page_id);
 int rimuru_page_place(rimuru_view_t view, int64_t page_id);
 int rimuru_page_free(rimuru_view_t view, int64_t page_id);
 
+/*
+ * Request-affine allocation (explainer page, memory-manager paragraph: the
+ * allocator tries to cut one request's small pages from the same parent page
+ * so that freeing them is simple).  Hands out the lowest free page cut from
+ * the same parent page as `hint_page` (e.g. the request's previous KV
+ * block).  hint_page == RIMURU_NEW_GROUP starts a group instead: the first
+ * page of a parent that has not been cut yet (so the group can merge back
+ * when it is freed).  When neither is possible, or hint_page == -1, it
+ * behaves as rimuru_page_alloc.
+ */
+#define RIMURU_NEW_GROUP (-2)
+int rimuru_page_alloc_near(rimuru_view_t view, int64_t hint_page, int64_t* page_id);
+
+/* Fragmentation of level `level` (>= 1): parents (pages of level - 1) that
+ * are split but still have free children, so cannot be merged back, and the
+ * number of such free children. */
+int rimuru_pool_fragmentation(rimuru_pool_t pool, int level, int64_t* partial_parents,
+                              int64_t* stranded_free);
+
 /* 1 if `page_id` of this view is currently owned by this view, else 0. */
 int rimuru_page_owned(rimuru_view_t view, int64_t page_id, int* owned);
 

@@ -45,6 +45,8 @@ struct Pool {
   int add_level(uint64_t page_bytes);       // keeps the chain ordered; returns its index
   // allocator primitives (caller holds mu)
   int alloc(int lvl, int32_t owner, int64_t* id);
+  // Prefer a free page cut from the same parent as `hint` (lowest id first).
+  int alloc_near(int lvl, int32_t owner, int64_t hint, int64_t* id);
   int place(int lvl, int32_t owner, int64_t id);
   int release(int lvl, int32_t owner, int64_t id);
   int split_page(int lvl, int64_t id);  // FREE page at lvl -> children FREE at lvl + 1

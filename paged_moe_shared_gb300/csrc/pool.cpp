@@ -115,6 +115,55 @@ int Pool::alloc(int lvl, int32_t owner_id, int64_t* id) {
   return RIMURU_OK;
 }
 
+int Pool::alloc_near(int lvl, int32_t owner_id, int64_t hint, int64_t* id) {
+  Level& L = levels[lvl];
+  if (lvl > 0 && hint == RIMURU_NEW_GROUP) {
+    // first page of a group: cut a parent that nobody uses yet, if there is one
+    Level& P = levels[lvl - 1];
+    int64_t parent = -1;
+    if (!P.free_list.empty()) {
+      parent = *P.free_list.begin();
+    } else if (lvl - 1 > 0) {  // cut a fresh parent out of the level above it
+      int st = alloc(lvl - 1, 0, &parent);
+      if (st != RIMURU_OK) parent = -1;
+      else {
+        P.state[parent] = Level::FREE;
+        P.owned -= 1;
+      }
+    }
+    if (parent >= 0) {
+      split_page(lvl - 1, parent);
+      const int64_t per = static_cast<int64_t>(P.page_bytes / L.page_bytes);
+      const int64_t c = parent * per;
+      L.free_list.erase(c);
+      L.state[c] = Level::OWNED;
+      L.owner[c] = owner_id;
+      L.owned += 1;
+      any_placed = true;
+      *id = c;
+      return RIMURU_OK;
+    }
+    clear_error();
+    return alloc(lvl, owner_id, id);
+  }
+  if (lvl > 0 && hint >= 0 && hint < L.n_pages) {
+    const int64_t per = static_cast<int64_t>(levels[lvl - 1].page_bytes / L.page_bytes);
+    const int64_t parent = hint / per;
+    for (int64_t c = parent * per; c < (parent + 1) * per; ++c) {
+      if (L.state[c] == Level::FREE) {
+        L.free_list.erase(c);
+        L.state[c] = Level::OWNED;
+        L.owner[c] = owner_id;
+        L.owned += 1;
+        any_placed = true;
+        *id = c;
+        return RIMURU_OK;
+      }
+    }
+  }
+  return alloc(lvl, owner_id, id);
+}
+
 int Pool::place(int lvl, int32_t owner_id, int64_t id) {
   Level& L = levels[lvl];
   if (id < 0 || id >= L.n_pages) return fail(RIMURU_ERR_RANGE, "page id out of range");
@@ -322,6 +371,40 @@ int rimuru_page_alloc(rimuru_view_t view, int64_t* page_id) {
   rimuru::View& v = view->v;
   std::lock_guard<std::mutex> g(v.pool->mu);
   return v.pool->alloc(v.pool->level_of(v.page_bytes), v.id, page_id);
+}
+
+int rimuru_page_alloc_near(rimuru_view_t view, int64_t hint_page, int64_t* page_id) {
+  rimuru::clear_error();
+  if (!view || !page_id) return fail(RIMURU_ERR_ARG, "null argument");
+  rimuru::View& v = view->v;
+  std::lock_guard<std::mutex> g(v.pool->mu);
+  return v.pool->alloc_near(v.pool->level_of(v.page_bytes), v.id, hint_page, page_id);
+}
+
+int rimuru_pool_fragmentation(rimuru_pool_t pool, int level, int64_t* partial_parents,
+                              int64_t* stranded_free) {
+  rimuru::clear_error();
+  if (!pool || !partial_parents || !stranded_free) return fail(RIMURU_ERR_ARG, "null argument");
+  rimuru::Pool& p = pool->p;
+  std::lock_guard<std::mutex> g(p.mu);
+  if (level < 1 || level >= static_cast<int>(p.levels.size()))
+    return fail(RIMURU_ERR_RANGE, "level must name a level that is cut from a parent");
+  const rimuru::Level& C = p.levels[level];
+  const rimuru::Level& P = p.levels[level - 1];
+  const int64_t per = static_cast<int64_t>(P.page_bytes / C.page_bytes);
+  int64_t partial = 0, stranded = 0;
+  for (int64_t q = 0; q < P.n_pages; ++q) {
+    if (P.state[q] != rimuru::Level::SPLIT) continue;
+    int64_t nfree = 0;
+    for (int64_t c = q * per; c < (q + 1) * per; ++c) nfree += (C.state[c] == rimuru::Level::FREE);
+    if (nfree > 0) {  // a split parent with free children cannot be merged back yet
+      partial += 1;
+      stranded += nfree;
+    }
+  }
+  *partial_parents = partial;
+  *stranded_free = stranded;
+  return RIMURU_OK;
 }
 
 int rimuru_page_place(rimuru_view_t view, int64_t page_id) {

@@ -26,6 +26,7 @@ ERR_STATE = -9
 ERR_UNSUPPORTED = -10
 
 PROJ_W1, PROJ_W3, PROJ_W2 = 0, 1, 2
+NEW_GROUP = -2
 DEV_OK, DEV_BAD_PAGE, DEV_NONFINITE, DEV_TIMEOUT, DEV_BAD_SHAPE = 0, 1, 2, 3, 4
 K_ROUTE, K_ALIGN, K_GATHER, K_GEMM1, K_GEMM2, K_COMBINE, K_COUNT = range(7)
 
@@ -42,6 +43,7 @@ EXPORTS = [
     "rimuru_profile_read", "rimuru_device_sm_count", "rimuru_selftest_bounded_wait",
     "rimuru_offload_create", "rimuru_offload_destroy", "rimuru_offload_prefetch",
     "rimuru_offload_forward", "rimuru_offload_stats", "rimuru_offload_resident",
+    "rimuru_page_alloc_near", "rimuru_pool_fragmentation",
 ]
 
 
@@ -86,6 +88,8 @@ def _load():
         "rimuru_view_info": ([P, ctypes.POINTER(i64), ctypes.POINTER(u64)], i32),
         "rimuru_page_alloc": ([P, ctypes.POINTER(i64)], i32),
         "rimuru_page_place": ([P, i64], i32),
+        "rimuru_page_alloc_near": ([P, i64, ctypes.POINTER(i64)], i32),
+        "rimuru_pool_fragmentation": ([P, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)], i32),
         "rimuru_page_free": ([P, i64], i32),
         "rimuru_page_owned": ([P, i64, ctypes.POINTER(i32)], i32),
         "rimuru_view_set_moe_shape": ([P, i32, i32, i32, i32, i32, i32], i32),
@@ -182,6 +186,18 @@ def rimuru_page_alloc(view) -> int:
     p = ctypes.c_int64()
     _check(lib.rimuru_page_alloc(view, ctypes.byref(p)))
     return p.value
+
+
+def rimuru_page_alloc_near(view, hint_page: int) -> int:
+    p = ctypes.c_int64()
+    _check(lib.rimuru_page_alloc_near(view, hint_page, ctypes.byref(p)))
+    return p.value
+
+
+def rimuru_pool_fragmentation(pool, level: int):
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib.rimuru_pool_fragmentation(pool, level, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
 
 
 def rimuru_page_place(view, page_id: int) -> None:

@@ -230,3 +230,65 @@ def test_forward_host_checks_run_before_any_device_work():
     R.rimuru_moe_forward(fake, fake, 0, ev, 0, fake, fake, 0)   # zero tokens: nothing to do
     R.rimuru_view_destroy(ev)
     R.rimuru_pool_destroy(pool)
+
+
+def _kv_pool():
+    pool = R.rimuru_pool_create(FAKE_BASE, 16 * 2 * MiB, 2 * MiB)
+    ev = R.rimuru_view_create(pool, 2 * MiB)
+    kv = R.rimuru_view_create(pool, 32 * KiB)   # 64 KV blocks per huge page
+    return pool, ev, kv
+
+
+@pytest.mark.parametrize("grouped", [False, True], ids=["plain", "grouped"])
+def test_request_affinity_lets_finished_requests_merge_back(grouped):
+    """Eight requests take 16 KV blocks each, interleaved one block at a time.  Grouped
+    (first block: a fresh parent; next blocks: near the previous one) keeps each request in
+    one parent, so freeing half of the requests returns whole huge pages; plain allocation
+    interleaves the requests in two parents and frees none."""
+    pool, ev, kv = _kv_pool()
+    blocks = {r: [] for r in range(8)}
+    for i in range(16):
+        for r in range(8):
+            if grouped:
+                hint = blocks[r][-1] if blocks[r] else R.NEW_GROUP
+                blocks[r].append(R.rimuru_page_alloc_near(kv, hint))
+            else:
+                blocks[r].append(R.rimuru_page_alloc(kv))
+    parents = {r: {b // 64 for b in blocks[r]} for r in range(8)}
+    if grouped:
+        assert all(len(p) == 1 for p in parents.values())
+        assert len(set().union(*parents.values())) == 8
+    for r in (0, 2, 4, 6):
+        for b in blocks[r]:
+            R.rimuru_page_free(kv, b)
+    s = stats(pool)
+    partial, stranded = R.rimuru_pool_fragmentation(pool, 1)
+    check_conservation(pool, 32 * MiB)
+    if grouped:
+        assert s[0]["pages_free"] == 16 - 4 and partial == 4 and stranded == 4 * 48
+        # the freed huge pages are whole again and can hold experts
+        for _ in range(12):
+            R.rimuru_page_alloc(ev)
+    else:
+        assert s[0]["pages_free"] == 14 and partial == 2 and stranded == 64
+    for r in (1, 3, 5, 7):
+        for b in blocks[r]:
+            R.rimuru_page_free(kv, b)
+    assert R.rimuru_pool_fragmentation(pool, 1) == (0, 0)
+    R.rimuru_view_destroy(kv)
+    R.rimuru_view_destroy(ev)
+    R.rimuru_pool_destroy(pool)
+
+
+def test_alloc_near_prefers_the_hint_parent():
+    pool, ev, kv = _kv_pool()
+    a = R.rimuru_page_alloc_near(kv, R.NEW_GROUP)
+    b = R.rimuru_page_alloc_near(kv, R.NEW_GROUP)
+    assert a // 64 != b // 64
+    c = R.rimuru_page_alloc_near(kv, a)
+    assert c // 64 == a // 64 and c != a
+    d = R.rimuru_page_alloc_near(kv, -1)   # plain: lowest free block
+    assert d == min(set(range(128)) - {a, b, c})
+    R.rimuru_view_destroy(kv)
+    R.rimuru_view_destroy(ev)
+    R.rimuru_pool_destroy(pool)
