@@ -382,6 +382,32 @@ int rimuru_offload_forward(rimuru_offload_t off, const void* x_bf16, const float
                            uint64_t workspace_bytes, void* stream);
 
 int rimuru_offload_stats(rimuru_offload_t off, rimuru_offload_counters* out);
+
+/* Change the number of resident experts.  Shrinking waits (on the host) for
+ * the cache's copies and for the last forward it recorded, evicts the least
+ * recently used slots and frees their pages (the allocator merges them back
+ * into huge pages); growing allocates pages of the view and adds empty
+ * slots.  RIMURU_ERR_OOM (nothing changed) when the pool cannot grow the
+ * cache.  Forwards must all run on one stream for the wait to cover them. */
+int rimuru_offload_resize(rimuru_offload_t off, int capacity_experts);
+int rimuru_offload_capacity(rimuru_offload_t off, int* capacity_experts);
+
+/*
+ * Workload-aware adjuster (Rimuru page, abstract and the explainer's
+ * paragraph on the adjuster: pages move between tensor types with runtime
+ * demand; the KV side grows when concurrency climbs and space returns to
+ * the experts when requests finish, in step with the prefetching pipeline).
+ * The pages give no policy; this one is: the KV view `kv_view` (same pool)
+ * is about to need `kv_blocks_wanted` free blocks.  Free KV blocks count
+ * first, then whole free huge pages; if they fall short the expert cache
+ * shrinks by enough slots (three huge pages each), and whole free huge
+ * pages beyond the KV need are given back to the cache, all within
+ * [min_capacity, max_capacity].  Requires expert pages equal to the huge
+ * page (the LCM rule gives that for both model shapes here).  Writes the
+ * resulting capacity.
+ */
+int rimuru_adjust(rimuru_offload_t off, rimuru_view_t kv_view, int64_t kv_blocks_wanted,
+                  int min_capacity, int max_capacity, int* capacity_out);
 /* Slot holding (layer, expert), or -1 when it is not resident. */
 int rimuru_offload_resident(rimuru_offload_t off, int layer, int expert, int* slot);
 

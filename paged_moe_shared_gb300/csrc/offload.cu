@@ -74,6 +74,7 @@ struct Offload {
   int stage_next = 0;
 
   rimuru_offload_counters st{};
+  rimuru_offload_counters& st_ = st;
 
   void unlink(int s) {
     if (prv[s] >= 0) nxt[prv[s]] = nxt[s]; else head = nxt[s];
@@ -141,6 +142,80 @@ struct Offload {
     ready_pending[layer] = 1;
     st.bytes_h2d += static_cast<int64_t>(3 * matrix_bytes);
     if (!demand) st.prefetch_loads += 1;
+    return RIMURU_OK;
+  }
+
+  // Wait (host) until no copy and no forward can still touch any slot.
+  int quiesce() {
+    cudaError_t e = cudaStreamSynchronize(copy);
+    if (e == cudaSuccess && seq > 0)
+      e = cudaEventSynchronize(done_ev[static_cast<size_t>(seq % kDoneRing)]);
+    return e == cudaSuccess ? RIMURU_OK : fail(RIMURU_ERR_CUDA, cuda_msg("waiting for the cache", e));
+  }
+
+  // Change the number of slots.  Shrinking drops the least recently used
+  // slots (evicting their experts) and frees their pages, which the
+  // allocator merges back into larger pages; growing takes new pages from the
+  // view's level and adds empty slots as the next victims.
+  int resize(int new_cap) {
+    if (new_cap == cap) return RIMURU_OK;
+    int st = quiesce();
+    if (st != RIMURU_OK) return st;
+    Pool& pool = *v->pool;
+    std::lock_guard<std::mutex> g(pool.mu);
+    const int lvl = pool.level_of(v->page_bytes);
+    std::vector<int> keep;  // surviving slots, most recent first
+    for (int s = head; s >= 0; s = nxt[s]) keep.push_back(s);
+    std::vector<int64_t> fresh;
+    if (new_cap < cap) {
+      for (int i = new_cap; i < cap; ++i) {
+        const int s = keep[i];
+        if (slot_key[s] >= 0) {
+          for (int p = 0; p < 3; ++p) set_entry(slot_key[s] / E, slot_key[s] % E, p, -1);
+          key_slot[slot_key[s]] = -1;
+          st_.evictions += 1;
+        }
+        for (int p = 0; p < 3; ++p) pool.release(lvl, v->id, slot_page[static_cast<size_t>(s) * 3 + p]);
+      }
+      keep.resize(new_cap);
+    } else {
+      for (int i = 0; i < 3 * (new_cap - cap); ++i) {
+        int64_t pg = -1;
+        if (pool.alloc(lvl, v->id, &pg) != RIMURU_OK) {
+          for (int64_t f : fresh) pool.release(lvl, v->id, f);
+          return fail(RIMURU_ERR_OOM, "the pool has no room for " + std::to_string(new_cap) +
+                                          " resident experts");
+        }
+        fresh.push_back(pg);
+      }
+    }
+    // rebuild the slot arrays in recency order; new empty slots go last
+    std::vector<int64_t> page2, seq2, op2;
+    std::vector<int> key2;
+    for (int s : keep) {
+      for (int p = 0; p < 3; ++p) page2.push_back(slot_page[static_cast<size_t>(s) * 3 + p]);
+      key2.push_back(slot_key[s]);
+      seq2.push_back(slot_seq[s]);
+      op2.push_back(slot_op[s]);
+    }
+    for (size_t i = 0; i < fresh.size(); i += 3) {
+      for (int p = 0; p < 3; ++p) page2.push_back(fresh[i + p]);
+      key2.push_back(-1);
+      seq2.push_back(-1);
+      op2.push_back(-1);
+    }
+    cap = new_cap;
+    slot_page.swap(page2);
+    slot_key.swap(key2);
+    slot_seq.swap(seq2);
+    slot_op.swap(op2);
+    prv.assign(cap, -1);
+    nxt.assign(cap, -1);
+    head = tail = -1;
+    for (int s = cap - 1; s >= 0; --s) push_front(s);  // slot 0 most recent
+    std::fill(key_slot.begin(), key_slot.end(), -1);
+    for (int s = 0; s < cap; ++s)
+      if (slot_key[s] >= 0) key_slot[slot_key[s]] = s;
     return RIMURU_OK;
   }
 
@@ -401,6 +476,56 @@ int rimuru_offload_forward(rimuru_offload_t off, const void* x_bf16, const float
   if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, rimuru::cuda_msg("completion event", e));
   for (int ex : routed) o.slot_seq[o.key_slot[layer * o.E + ex]] = o.seq;
   o.st.forwards += 1;
+  return RIMURU_OK;
+}
+
+int rimuru_offload_resize(rimuru_offload_t off, int capacity_experts) {
+  rimuru::clear_error();
+  if (!off) return fail(RIMURU_ERR_ARG, "null handle");
+  rimuru::Offload& o = off->o;
+  if (capacity_experts <= 0 || capacity_experts > o.L * o.E)
+    return fail(RIMURU_ERR_ARG, "capacity must be in [1, layers * experts]");
+  return o.resize(capacity_experts);
+}
+
+int rimuru_offload_capacity(rimuru_offload_t off, int* capacity_experts) {
+  rimuru::clear_error();
+  if (!off || !capacity_experts) return fail(RIMURU_ERR_ARG, "null argument");
+  *capacity_experts = off->o.cap;
+  return RIMURU_OK;
+}
+
+int rimuru_adjust(rimuru_offload_t off, rimuru_view_t kv_view, int64_t kv_blocks_wanted,
+                  int min_capacity, int max_capacity, int* capacity_out) {
+  rimuru::clear_error();
+  if (!off || !kv_view || !capacity_out) return fail(RIMURU_ERR_ARG, "null argument");
+  rimuru::Offload& o = off->o;
+  rimuru::View& kv = kv_view->v;
+  rimuru::Pool& pool = *o.v->pool;
+  if (kv.pool != &pool) return fail(RIMURU_ERR_ARG, "the KV view belongs to another pool");
+  if (o.v->page_bytes != pool.huge_page_bytes)
+    return fail(RIMURU_ERR_UNSUPPORTED, "the adjuster needs expert pages equal to huge pages");
+  if (kv_blocks_wanted < 0 || min_capacity < 1 || max_capacity < min_capacity ||
+      max_capacity > o.L * o.E)
+    return fail(RIMURU_ERR_ARG, "bad demand or capacity bounds");
+  int64_t free_huge = 0, kv_free = 0;
+  {
+    std::lock_guard<std::mutex> g(pool.mu);
+    free_huge = static_cast<int64_t>(pool.levels[0].free_list.size());
+    const int lk = pool.level_of(kv.page_bytes);
+    if (lk > 0) kv_free = static_cast<int64_t>(pool.levels[lk].free_list.size());
+  }
+  const int64_t per_huge = static_cast<int64_t>(pool.huge_page_bytes / kv.page_bytes);
+  const int64_t need_blocks = std::max<int64_t>(0, kv_blocks_wanted - kv_free);
+  const int64_t need_huge = (need_blocks + per_huge - 1) / per_huge;
+  const int64_t spare = free_huge - need_huge;  // huge pages beyond what KV will take
+  int64_t target = o.cap;
+  if (spare < 0) target = o.cap - (-spare + 2) / 3;  // each slot frees three huge pages
+  else target = o.cap + spare / 3;
+  target = std::max<int64_t>(min_capacity, std::min<int64_t>(max_capacity, target));
+  int st = o.resize(static_cast<int>(target));
+  if (st != RIMURU_OK) return st;
+  *capacity_out = o.cap;
   return RIMURU_OK;
 }
 

@@ -43,7 +43,8 @@ EXPORTS = [
     "rimuru_profile_read", "rimuru_device_sm_count", "rimuru_selftest_bounded_wait",
     "rimuru_offload_create", "rimuru_offload_destroy", "rimuru_offload_prefetch",
     "rimuru_offload_forward", "rimuru_offload_stats", "rimuru_offload_resident",
-    "rimuru_page_alloc_near", "rimuru_pool_fragmentation",
+    "rimuru_page_alloc_near", "rimuru_pool_fragmentation", "rimuru_offload_resize",
+    "rimuru_offload_capacity", "rimuru_adjust",
 ]
 
 
@@ -112,6 +113,9 @@ def _load():
         "rimuru_offload_forward": ([P, P, P, i32, i32, P, P, u64, P], i32),
         "rimuru_offload_stats": ([P, ctypes.POINTER(OffloadCounters)], i32),
         "rimuru_offload_resident": ([P, i32, i32, ctypes.POINTER(i32)], i32),
+        "rimuru_offload_resize": ([P, i32], i32),
+        "rimuru_offload_capacity": ([P, ctypes.POINTER(i32)], i32),
+        "rimuru_adjust": ([P, P, i64, i32, i32, ctypes.POINTER(i32)], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -336,3 +340,20 @@ def rimuru_offload_resident(off, layer: int, expert: int) -> int:
     s = ctypes.c_int()
     _check(lib.rimuru_offload_resident(off, layer, expert, ctypes.byref(s)))
     return s.value
+
+
+def rimuru_offload_resize(off, capacity_experts: int) -> None:
+    _check(lib.rimuru_offload_resize(off, capacity_experts))
+
+
+def rimuru_offload_capacity(off) -> int:
+    c = ctypes.c_int()
+    _check(lib.rimuru_offload_capacity(off, ctypes.byref(c)))
+    return c.value
+
+
+def rimuru_adjust(off, kv_view, kv_blocks_wanted: int, min_capacity: int, max_capacity: int) -> int:
+    c = ctypes.c_int()
+    _check(lib.rimuru_adjust(off, kv_view, kv_blocks_wanted, min_capacity, max_capacity,
+                             ctypes.byref(c)))
+    return c.value
