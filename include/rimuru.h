@@ -248,6 +248,8 @@ typedef struct rimuru_ws_layout {
   uint64_t x_sorted;   /* bf16 [A][hidden]: x rows in sorted order */
   uint64_t h;          /* bf16 [A][inter]: silu(x w1) * (x w3) in sorted order */
   uint64_t y;          /* bf16 [A][hidden]: h w2 in sorted order (unweighted) */
+  uint64_t tile_cnt;   /* int32 [2][...]: split-K tile counters of the two GEMMs */
+  uint64_t part;       /* fp32 split-K partial tiles (empty when no GEMM is split) */
   uint64_t total;      /* bytes needed */
   int32_t chunks;      /* number of routing chunks */
   int32_t max_tiles;   /* capacity of the tile table */

@@ -193,6 +193,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 // silu(g) * u with silu(g) = g / (1 + e^-g).  The result is rounded to bf16,
 // so the fast exponential and division (a few ulp of fp32) are far below that
 // rounding; for g < -87 the denominator overflows and the result is 0.
+// Named barrier 1 over the 128 epilogue threads of the GEMM kernels.
+__device__ __forceinline__ void named_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// The same barrier, returning whether the predicate holds in all 128 threads.
+__device__ __forceinline__ bool named_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "setp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, 1, 128, a;\n\t"
+      "selp.u32 %0, 1, 0, b;\n\t}\n"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }

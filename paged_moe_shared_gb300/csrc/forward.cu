@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -72,6 +73,15 @@ void layout_for(const View& v, int T, rimuru_ws_layout* L) {
   L->x_sorted = take(A * v.hidden * 2);
   L->h = take(A * v.inter * 2);
   L->y = take(A * v.hidden * 2);
+  // split-K bookkeeping (see split_count): counters for both GEMMs, one slab
+  // of fp32 partials per work unit, sized for the larger of the two
+  const long long t1 = static_cast<long long>(max_tiles) * (v.inter / 128);
+  const long long t2 = static_cast<long long>(max_tiles) * (v.hidden / 256);
+  const int s1 = split_count(t1, v.hidden / 64), s2 = split_count(t2, v.inter / 64);
+  const uint64_t part_rows = A < static_cast<uint64_t>(kTileM) ? A : kTileM;
+  const uint64_t units = std::max<uint64_t>(s1 > 1 ? t1 * s1 : 0, s2 > 1 ? t2 * s2 : 0);
+  L->tile_cnt = take(2 * std::max<uint64_t>(t1, t2) * 4);
+  L->part = take(units * part_rows * 256 * 4);
   L->total = at;
   L->chunks = chunks;
   L->max_tiles = static_cast<int32_t>(max_tiles);

@@ -16,6 +16,23 @@ constexpr int kTileM = 128;         // rows (assignments) per GEMM tile
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
 
+// Split-K for layers with few tiles: the K range of a tile is cut into S
+// parts computed by different CTAs (fp32 partials in the workspace, summed
+// in split order by the last CTA to finish the tile).  S is chosen from an
+// upper bound of the tile count so the workspace size does not depend on
+// the device: about kSplitTarget work units (two waves of a 152-SM GPU),
+// only when the tiles fill less than half a wave, and at least
+// kMinSplitBlocks k blocks per split (shorter splits cost more in the
+// pipeline fill and the reduction than they save).
+constexpr int kSplitTarget = 304;
+constexpr int kMinSplitBlocks = 8;
+inline int split_count(long long tiles_ub, int nkb) {
+  if (tiles_ub <= 0 || tiles_ub * 4 > kSplitTarget) return 1;
+  long long s = kSplitTarget / tiles_ub;
+  if (s > nkb / kMinSplitBlocks) s = nkb / kMinSplitBlocks;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
 // Tokens routed by one CTA (one warp each); their k assignments form one chunk.
 inline int tokens_per_chunk(int k) {
   return kRouteWarps * k <= kChunkAssign ? kRouteWarps : kChunkAssign / k;
@@ -35,9 +52,11 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
 
 // a2: offsets, stable expert-sorted permutation, its inverse and the 128-row
 // tile table.  One CTA per routing chunk.
+// Also zeroes the split-K tile counters (cnt_len ints at tile_cnt).
 cudaError_t launch_align(const int32_t* ids, const int32_t* chunk_hist, int chunks, int A, int E,
                          int chunk, int32_t* offsets, int32_t* sorted, int32_t* inv,
-                         int32_t* tiles, int32_t* num_tiles, int* err, const LaunchOpts& o);
+                         int32_t* tiles, int32_t* num_tiles, int32_t* tile_cnt, int cnt_len,
+                         int* err, const LaunchOpts& o);
 
 // x rows in expert-sorted order: x_sorted[r] = x[sorted[r] / k].
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted, int A, int k, int H,
@@ -56,6 +75,10 @@ struct GemmArgs {
   int max_tiles;              // upper bound of num_tiles (grid sizing)
   int weights_evict_first;    // 1: weights are streamed once (decode-sized batches)
   int* err;
+  int splits;                 // split-K parts per tile (1: no split)
+  int part_rows;              // rows of one partial slab (>= rows of any tile)
+  float* part;                // [tiles * splits][part_rows][256] fp32 partials
+  int32_t* tile_cnt;          // [tiles] finished splits per tile (zeroed by align)
 };
 
 // a3: h = silu(x_sorted w1_e) * (x_sorted w3_e); w1/w3 read in place from pages.

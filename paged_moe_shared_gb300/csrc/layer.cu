@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <string>
 
@@ -71,8 +72,8 @@ int make_weight_maps(void* pool_base, uint64_t page_bytes, int64_t n_pages, int 
 namespace {
 
 struct LayerPtrs {
-  int32_t *ids, *chunk_hist, *offsets, *sorted, *inv, *tiles, *num_tiles;
-  float* w;
+  int32_t *ids, *chunk_hist, *offsets, *sorted, *inv, *tiles, *num_tiles, *tile_cnt;
+  float *w, *part;
   __nv_bfloat16 *xs, *h, *y;
 };
 
@@ -91,7 +92,23 @@ LayerPtrs pointers_of(const LayerLaunch& a) {
   q.xs = reinterpret_cast<__nv_bfloat16*>(ws + L.x_sorted);
   q.h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
   q.y = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
+  q.tile_cnt = reinterpret_cast<int32_t*>(ws + L.tile_cnt);
+  q.part = reinterpret_cast<float*>(ws + L.part);
   return q;
+}
+
+// Tile-count upper bounds and split-K parts of the two GEMMs (as in the layout).
+struct Splits {
+  long long t1, t2;
+  int s1, s2;
+};
+Splits splits_of(const LayerLaunch& a) {
+  Splits s;
+  s.t1 = static_cast<long long>(a.layout.max_tiles) * (a.I / 128);
+  s.t2 = static_cast<long long>(a.layout.max_tiles) * (a.H / 256);
+  s.s1 = split_count(s.t1, a.H / 64);
+  s.s2 = split_count(s.t2, a.I / 64);
+  return s;
 }
 
 }  // namespace
@@ -117,7 +134,8 @@ int launch_layer_route(const LayerLaunch& a) {
   mark(RIMURU_K_ALIGN, 0);
   if (e == cudaSuccess)
     e = launch_align(q.ids, q.chunk_hist, a.layout.chunks, a.T * a.k, a.E, tpc * a.k, q.offsets,
-                     q.sorted, q.inv, q.tiles, q.num_tiles, a.err, next);
+                     q.sorted, q.inv, q.tiles, q.num_tiles, q.tile_cnt,
+                     static_cast<int>(2 * std::max(splits_of(a).t1, splits_of(a).t2)), a.err, next);
   mark(RIMURU_K_ALIGN, 1);
   if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, cuda_msg("kernel launch", e));
   return RIMURU_OK;
@@ -152,7 +170,14 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route) {
   g1.max_tiles = L.max_tiles;
   g1.weights_evict_first = (A <= E * kTileM / 4) ? 1 : 0;
   g1.err = a.err;
+  const Splits sp = splits_of(a);
+  g1.part_rows = A < kTileM ? A : kTileM;
+  g1.part = q.part;
   GemmArgs g2 = g1;
+  g1.splits = sp.s1;
+  g1.tile_cnt = q.tile_cnt;
+  g2.splits = sp.s2;
+  g2.tile_cnt = q.tile_cnt + std::max(sp.t1, sp.t2);
   g1.out = q.h;
   g1.ldo = I;
   g1.n_blocks = I / 128;

@@ -56,6 +56,7 @@ struct Shared {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int last;  // split-K: this CTA finished the last split of the current tile
 };
 
 template <bool kSwiGLU>
@@ -98,7 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   grid_dep_wait();  // tile table, offsets and activations come from earlier kernels
   grid_dep_launch();  // the next kernel may be scheduled now; it waits for our completion
-  const int n_tiles = *p.num_tiles * p.n_blocks;
+  const int S = p.splits;
+  const int n_units = *p.num_tiles * p.n_blocks * S;  // (tile, split) work units
   const int nkb = p.num_k_blocks;
 
   if (warp == 0) {
@@ -108,7 +110,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_a = policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const int tile = u / S, split = u - tile * S;
+        const int kb0 = split * nkb / S, kb1 = (split + 1) * nkb / S;
         const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
         const int e = p.tiles[2 * mb], row0 = p.tiles[2 * mb + 1];
         int pg0, pg1, n0;
@@ -124,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           set_error(p.err, RIMURU_DEV_BAD_PAGE);  // host checks make this unreachable
           pg0 = pg1 = 0;
         }
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
           if (!mbar_wait(&sh->empty[s], ph ^ 1u, abort)) {
             ok = false;
@@ -161,7 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true);
       uint32_t it = 0, local = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++local) {
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++local) {
+        const int split = u % S;
+        const int kb0 = split * nkb / S, kb1 = (split + 1) * nkb / S;
         const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
         if (!mbar_wait(&sh->tempty[acc], aph ^ 1u, abort)) {
           ok = false;
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
           if (!mbar_wait(&sh->full[s], ph, abort)) {
             ok = false;
@@ -185,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // B: MN-major, 64-column chunks kBChunk apart (LBO), 8-k-row groups
             // 1024 B apart (SBO); +16 rows * 128 B per 16 k.
             const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kBChunk, 1024);
-            umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16(d, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
           }
           umma_commit(&sh->empty[s]);  // stage s is free once these MMAs are done
         }
@@ -205,9 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may read
     uint32_t local = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+    const int et = (warp - 2) * 32 + lane;  // 0..127 across the epilogue warps
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++local) {
+      const int tile = u / S;
       const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
-      const bool got = mbar_wait(&sh->tfull[acc], aph, abort);
+      bool got = mbar_wait(&sh->tfull[acc], aph, abort);
+      if (S > 1) got = named_bar_and(got);  // the split path syncs the four warps: decide together
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) {
           set_error(p.err, RIMURU_DEV_TIMEOUT);
@@ -220,7 +229,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = p.tiles[2 * mb], row0 = p.tiles[2 * mb + 1];
       const int rows = min(BM, p.offsets[e + 1] - row0);
       const uint32_t tb = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-      if (kSwiGLU) {
+      if (S > 1) {
+        // Split-K: write this split's fp32 accumulator rows to its slab, count
+        // the tile's finished splits, and let the last CTA sum the slabs in
+        // split order (deterministic) and apply the epilogue.
+        const int r = q * 32 + lane;
+        float* slab = p.part + static_cast<size_t>(u) * p.part_rows * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t a[32];
+          tmem_ld32(tb + c0, a);
+          tmem_ld_wait();
+          if (r < rows) {
+            float4* dst = reinterpret_cast<float4*>(slab + static_cast<size_t>(r) * BN + c0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(a[4 * v]), __uint_as_float(a[4 * v + 1]),
+                                   __uint_as_float(a[4 * v + 2]), __uint_as_float(a[4 * v + 3]));
+          }
+        }
+        __threadfence();
+        named_bar_sync();
+        if (et == 0) sh->last = (atomicAdd(&p.tile_cnt[tile], 1) == S - 1);
+        named_bar_sync();
+        if (sh->last) {
+          __threadfence();
+          const float* base = p.part + static_cast<size_t>(tile) * S * p.part_rows * BN;
+          const size_t slab_elems = static_cast<size_t>(p.part_rows) * BN;
+          if (kSwiGLU) {
+            const int n0 = nb * (BN / 2);
+            for (int idx = et; idx < rows * (BN / 2); idx += 128) {
+              const int rr = idx / (BN / 2), c = idx % (BN / 2);
+              float g = 0.f, v = 0.f;
+              for (int sp = 0; sp < S; ++sp) {
+                const float* row = base + sp * slab_elems + static_cast<size_t>(rr) * BN;
+                g += __ldcg(row + c);
+                v += __ldcg(row + BN / 2 + c);
+              }
+              p.out[static_cast<size_t>(row0 + rr) * p.ldo + n0 + c] =
+                  __float2bfloat16_rn(silu_mul(g, v));
+            }
+          } else {
+            const int n0 = nb * BN;
+            for (int idx = et; idx < rows * BN; idx += 128) {
+              const int rr = idx / BN, c = idx % BN;
+              float y = 0.f;
+              for (int sp = 0; sp < S; ++sp)
+                y += __ldcg(base + sp * slab_elems + static_cast<size_t>(rr) * BN + c);
+              p.out[static_cast<size_t>(row0 + rr) * p.ldo + n0 + c] = __float2bfloat16_rn(y);
+            }
+          }
+        }
+      } else if (kSwiGLU) {
         // GEMM 1: each lane writes its own row of h, 32 columns at a time.
         const int r = q * 32 + lane;
         const bool valid = r < rows;
@@ -313,7 +373,7 @@ cudaError_t launch_gemm(const CUtensorMap& tm_act, const CUtensorMap& tm_w, cons
     if (st != cudaSuccess) return st;
     configured = true;
   }
-  const long long tiles = static_cast<long long>(a.max_tiles) * a.n_blocks;
+  const long long tiles = static_cast<long long>(a.max_tiles) * a.n_blocks * a.splits;
   const int grid = static_cast<int>(tiles < o.sm_count ? tiles : o.sm_count);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid > 0 ? grid : 1);

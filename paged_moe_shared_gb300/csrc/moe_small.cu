@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ chunk_hist, int chunks, int A,
     int E, int chunk, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted,
     int32_t* __restrict__ inv, int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles,
-    int* err) {
+    int32_t* __restrict__ tile_cnt, int cnt_len, int* err) {
   __shared__ int s_part_tot[kChunkAssign];
   __shared__ int s_part_bef[kChunkAssign];
   __shared__ int s_base[kMaxExperts];
@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
   const int off = block_exclusive_scan(tot, s_warp);
   if (tid < E) s_base[tid] = off + before;
   if (c == 0) {
+    for (int i = tid; i < cnt_len; i += blockDim.x) tile_cnt[i] = 0;
     if (tid < E) offsets[tid] = off;
     if (tid == E - 1) offsets[E] = off + tot;
     const int nb = (tot + kTileM - 1) / kTileM;
@@ -331,9 +332,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
 
 cudaError_t launch_align(const int32_t* ids, const int32_t* chunk_hist, int chunks, int A, int E,
                          int chunk, int32_t* offsets, int32_t* sorted, int32_t* inv,
-                         int32_t* tiles, int32_t* num_tiles, int* err, const LaunchOpts& o) {
+                         int32_t* tiles, int32_t* num_tiles, int32_t* tile_cnt, int cnt_len,
+                         int* err, const LaunchOpts& o) {
   return launch(moe_align_kernel, dim3(chunks), dim3(kChunkAssign), 0, o, ids, chunk_hist, chunks,
-                A, E, chunk, offsets, sorted, inv, tiles, num_tiles, err);
+                A, E, chunk, offsets, sorted, inv, tiles, num_tiles, tile_cnt, cnt_len, err);
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted, int A, int k, int H,

@@ -211,3 +211,30 @@ def test_q35_mixed_pool_4096_sampled(oracle):
     w = wl.q35_mixed_pool(0, T=4096)
     tokens = np.sort(np.random.default_rng(1).choice(w.T, 32, replace=False))
     check(run_gpu(w), w, run_oracle(oracle, w, tokens=tokens), tokens=tokens)
+
+
+def _wide_inter_t1():
+    # I = 1024 gives GEMM 2 sixteen k blocks, enough for it to split too
+    shape = wl.MoEShape(H=256, I=1024, E=4, k=1)
+    return wl.build_simple("wide_inter", shape, 1, pool_pages=16, seed=9)
+
+
+@pytest.mark.parametrize("make", [lambda: wl.q35_mixed_pool(0, T=1), lambda: wl.q3_decode(0, T=1),
+                                  _wide_inter_t1],
+                         ids=["q35_T1_gemm1_split", "q3_T1_gemm1_split", "wide_inter_gemm2_split"])
+def test_split_k_is_used_for_few_tiles_and_is_deterministic(oracle, make):
+    """With few tiles the GEMMs split K over several CTAs and sum the fp32 partials in split
+    order, so repeated forwards agree bit for bit."""
+    w = make()
+    r = Runner(w)
+    try:
+        assert r.layout["total"] > r.layout["part"]  # a partial-sum region exists
+        r.forward()
+        a = r.results()
+        r.forward()
+        b = r.results()
+    finally:
+        r.close()
+    check(a, w, run_oracle(oracle, w))
+    for key in ("out", "h", "y"):
+        assert np.array_equal(a[key], b[key]), key
