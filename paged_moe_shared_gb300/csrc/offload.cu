@@ -76,6 +76,31 @@ struct Offload {
   rimuru_offload_counters st{};
   rimuru_offload_counters& st_ = st;
 
+  // Copies are merged while both ends continue the pending run.
+  uint64_t pend_dst = 0, pend_src = 0, pend_len = 0;
+  int64_t waited_seq = 0;  // the copy stream already waits for forwards up to this one
+
+  cudaError_t flush() {
+    if (pend_len == 0) return cudaSuccess;
+    uint8_t* pool = static_cast<uint8_t*>(v->pool->base);
+    cudaError_t e = cudaMemcpyAsync(pool + pend_dst, host + pend_src, pend_len,
+                                    cudaMemcpyHostToDevice, copy);
+    pend_len = 0;
+    return e;
+  }
+  cudaError_t queue_copy(uint64_t dst, uint64_t src, uint64_t len) {
+    if (pend_len && dst == pend_dst + pend_len && src == pend_src + pend_len &&
+        len == v->page_bytes) {
+      pend_len += len;
+      return cudaSuccess;
+    }
+    cudaError_t e = flush();
+    pend_dst = dst;
+    pend_src = src;
+    pend_len = len;
+    return e;
+  }
+
   void unlink(int s) {
     if (prv[s] >= 0) nxt[prv[s]] = nxt[s]; else head = nxt[s];
     if (nxt[s] >= 0) prv[nxt[s]] = prv[s]; else tail = prv[s];
@@ -124,13 +149,16 @@ struct Offload {
       st.evictions += 1;
     }
     cudaError_t err = cudaSuccess;
-    if (slot_seq[s] >= 0)
-      err = cudaStreamWaitEvent(copy, done_ev[static_cast<size_t>(slot_seq[s] % kDoneRing)], 0);
-    uint8_t* pool = static_cast<uint8_t*>(v->pool->base);
+    if (slot_seq[s] > waited_seq) {  // a forward newer than any waited for read this slot
+      err = flush();
+      if (err == cudaSuccess)
+        err = cudaStreamWaitEvent(copy, done_ev[static_cast<size_t>(slot_seq[s] % kDoneRing)], 0);
+      waited_seq = slot_seq[s];
+    }
     for (int p = 0; p < 3 && err == cudaSuccess; ++p) {
       const uint64_t dst = static_cast<uint64_t>(slot_page[static_cast<size_t>(s) * 3 + p]) * v->page_bytes;
       const uint64_t src = (static_cast<uint64_t>(key) * 3 + p) * v->page_bytes;
-      err = cudaMemcpyAsync(pool + dst, host + src, matrix_bytes, cudaMemcpyHostToDevice, copy);
+      err = queue_copy(dst, src, matrix_bytes);
     }
     if (err != cudaSuccess) return fail(RIMURU_ERR_CUDA, cuda_msg("expert copy", err));
     for (int p = 0; p < 3; ++p)
@@ -147,7 +175,8 @@ struct Offload {
 
   // Wait (host) until no copy and no forward can still touch any slot.
   int quiesce() {
-    cudaError_t e = cudaStreamSynchronize(copy);
+    cudaError_t e = flush();
+    if (e == cudaSuccess) e = cudaStreamSynchronize(copy);
     if (e == cudaSuccess && seq > 0)
       e = cudaEventSynchronize(done_ev[static_cast<size_t>(seq % kDoneRing)]);
     return e == cudaSuccess ? RIMURU_OK : fail(RIMURU_ERR_CUDA, cuda_msg("waiting for the cache", e));
@@ -220,7 +249,8 @@ struct Offload {
   }
 
   int mark_ready(int layer) {
-    cudaError_t e = cudaEventRecord(ready_ev[layer], copy);
+    cudaError_t e = flush();
+    if (e == cudaSuccess) e = cudaEventRecord(ready_ev[layer], copy);
     return e == cudaSuccess ? RIMURU_OK : fail(RIMURU_ERR_CUDA, cuda_msg("copy event", e));
   }
 };
