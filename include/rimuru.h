@@ -248,6 +248,8 @@ typedef struct rimuru_ws_layout {
   uint64_t x_sorted;   /* bf16 [A][hidden]: x rows in sorted order */
   uint64_t h;          /* bf16 [A][inter]: silu(x w1) * (x w3) in sorted order */
   uint64_t y;          /* bf16 [A][hidden]: h w2 in sorted order (unweighted) */
+  uint64_t ptiles;     /* int32 [max_tiles][2]: (expert, first row) of each 256-row pair of blocks */
+  uint64_t num_ptiles; /* int32: number of valid pair entries */
   uint64_t tile_cnt;   /* int32 [2][...]: split-K tile counters of the two GEMMs */
   uint64_t part;       /* fp32 split-K partial tiles (empty when no GEMM is split) */
   uint64_t total;      /* bytes needed */

@@ -80,6 +80,8 @@ void layout_for(const View& v, int T, rimuru_ws_layout* L) {
   const int s1 = split_count(t1, v.hidden / 64), s2 = split_count(t2, v.inter / 64);
   const uint64_t part_rows = A < static_cast<uint64_t>(kTileM) ? A : kTileM;
   const uint64_t units = std::max<uint64_t>(s1 > 1 ? t1 * s1 : 0, s2 > 1 ? t2 * s2 : 0);
+  L->ptiles = take(max_tiles * 2 * 4);
+  L->num_ptiles = take(16);
   L->tile_cnt = take(2 * std::max<uint64_t>(t1, t2) * 4);
   L->part = take(units * part_rows * 256 * 4);
   L->total = at;

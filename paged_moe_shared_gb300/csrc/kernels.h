@@ -52,11 +52,13 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
 
 // a2: offsets, stable expert-sorted permutation, its inverse and the 128-row
 // tile table.  One CTA per routing chunk.
-// Also zeroes the split-K tile counters (cnt_len ints at tile_cnt).
+// Also writes the table of 256-row pairs of blocks (ptiles) and zeroes the
+// split-K tile counters (cnt_len ints at tile_cnt).
 cudaError_t launch_align(const int32_t* ids, const int32_t* chunk_hist, int chunks, int A, int E,
                          int chunk, int32_t* offsets, int32_t* sorted, int32_t* inv,
-                         int32_t* tiles, int32_t* num_tiles, int32_t* tile_cnt, int cnt_len,
-                         int* err, const LaunchOpts& o);
+                         int32_t* tiles, int32_t* num_tiles, int32_t* ptiles,
+                         int32_t* num_ptiles, int32_t* tile_cnt, int cnt_len, int* err,
+                         const LaunchOpts& o);
 
 // x rows in expert-sorted order: x_sorted[r] = x[sorted[r] / k].
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted, int A, int k, int H,
@@ -84,6 +86,14 @@ struct GemmArgs {
 // a3: h = silu(x_sorted w1_e) * (x_sorted w3_e); w1/w3 read in place from pages.
 cudaError_t launch_gemm1_swiglu(const CUtensorMap& tm_x, const CUtensorMap& tm_w13,
                                 const GemmArgs& a, const LaunchOpts& o);
+// a3 for large batches: the same GEMM with two row blocks of an expert per CTA
+// sharing each weight tile (tiles/num_tiles in `a` name the pair table).
+cudaError_t launch_gemm1_swiglu_paired(const CUtensorMap& tm_x, const CUtensorMap& tm_w13,
+                                       const GemmArgs& a, const LaunchOpts& o);
+// Use the paired GEMM 1 when the assignments average at least this many
+// 128-row blocks per expert (most experts then have pairs of blocks).
+constexpr int kPairMinBlocksPerExpert = 2;
+
 // a4: y = h w2_e; w2 read in place from its page.
 cudaError_t launch_gemm2(const CUtensorMap& tm_h, const CUtensorMap& tm_w2, const GemmArgs& a,
                          const LaunchOpts& o);

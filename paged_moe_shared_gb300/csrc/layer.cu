@@ -72,7 +72,8 @@ int make_weight_maps(void* pool_base, uint64_t page_bytes, int64_t n_pages, int 
 namespace {
 
 struct LayerPtrs {
-  int32_t *ids, *chunk_hist, *offsets, *sorted, *inv, *tiles, *num_tiles, *tile_cnt;
+  int32_t *ids, *chunk_hist, *offsets, *sorted, *inv, *tiles, *num_tiles, *ptiles, *num_ptiles,
+      *tile_cnt;
   float *w, *part;
   __nv_bfloat16 *xs, *h, *y;
 };
@@ -92,6 +93,8 @@ LayerPtrs pointers_of(const LayerLaunch& a) {
   q.xs = reinterpret_cast<__nv_bfloat16*>(ws + L.x_sorted);
   q.h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
   q.y = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
+  q.ptiles = reinterpret_cast<int32_t*>(ws + L.ptiles);
+  q.num_ptiles = reinterpret_cast<int32_t*>(ws + L.num_ptiles);
   q.tile_cnt = reinterpret_cast<int32_t*>(ws + L.tile_cnt);
   q.part = reinterpret_cast<float*>(ws + L.part);
   return q;
@@ -134,7 +137,7 @@ int launch_layer_route(const LayerLaunch& a) {
   mark(RIMURU_K_ALIGN, 0);
   if (e == cudaSuccess)
     e = launch_align(q.ids, q.chunk_hist, a.layout.chunks, a.T * a.k, a.E, tpc * a.k, q.offsets,
-                     q.sorted, q.inv, q.tiles, q.num_tiles, q.tile_cnt,
+                     q.sorted, q.inv, q.tiles, q.num_tiles, q.ptiles, q.num_ptiles, q.tile_cnt,
                      static_cast<int>(2 * std::max(splits_of(a).t1, splits_of(a).t2)), a.err, next);
   mark(RIMURU_K_ALIGN, 1);
   if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, cuda_msg("kernel launch", e));
@@ -203,7 +206,18 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route) {
     e = launch_gather(static_cast<const __nv_bfloat16*>(a.x), q.sorted, A, k, H, q.xs, gather_o);
   mark(RIMURU_K_GATHER, 1);
   mark(RIMURU_K_GEMM1, 0);
-  if (e == cudaSuccess) e = launch_gemm1_swiglu(tm_x, *a.tm_w13, g1, o);
+  const bool paired = sp.s1 == 1 &&
+                      static_cast<long long>(A) >= static_cast<long long>(kPairMinBlocksPerExpert) * kTileM * E;
+  if (e == cudaSuccess) {
+    if (paired) {
+      GemmArgs gp = g1;
+      gp.tiles = q.ptiles;
+      gp.num_tiles = q.num_ptiles;
+      e = launch_gemm1_swiglu_paired(tm_x, *a.tm_w13, gp, o);
+    } else {
+      e = launch_gemm1_swiglu(tm_x, *a.tm_w13, g1, o);
+    }
+  }
   mark(RIMURU_K_GEMM1, 1);
   mark(RIMURU_K_GEMM2, 0);
   if (e == cudaSuccess) e = launch_gemm2(tm_h, *a.tm_w2, g2, o);

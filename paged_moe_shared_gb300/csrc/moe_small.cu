@@ -167,7 +167,8 @@ __global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ chunk_hist, int chunks, int A,
     int E, int chunk, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted,
     int32_t* __restrict__ inv, int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles,
-    int32_t* __restrict__ tile_cnt, int cnt_len, int* err) {
+    int32_t* __restrict__ ptiles, int32_t* __restrict__ num_ptiles, int32_t* __restrict__ tile_cnt,
+    int cnt_len, int* err) {
   __shared__ int s_part_tot[kChunkAssign];
   __shared__ int s_part_bef[kChunkAssign];
   __shared__ int s_base[kMaxExperts];
@@ -217,6 +218,15 @@ __global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
       }
     }
     if (tid == E - 1) *num_tiles = first + nb;
+    const int np = (nb + 1) / 2;  // pairs of blocks, the last one possibly alone
+    const int pfirst = block_exclusive_scan(np, s_warp);
+    if (tid < E) {
+      for (int b = 0; b < np; ++b) {
+        ptiles[2 * (pfirst + b)] = tid;
+        ptiles[2 * (pfirst + b) + 1] = off + b * 2 * kTileM;
+      }
+    }
+    if (tid == E - 1) *num_ptiles = pfirst + np;
   }
   __syncthreads();
   if (tid < n) {
@@ -332,10 +342,12 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
 
 cudaError_t launch_align(const int32_t* ids, const int32_t* chunk_hist, int chunks, int A, int E,
                          int chunk, int32_t* offsets, int32_t* sorted, int32_t* inv,
-                         int32_t* tiles, int32_t* num_tiles, int32_t* tile_cnt, int cnt_len,
-                         int* err, const LaunchOpts& o) {
+                         int32_t* tiles, int32_t* num_tiles, int32_t* ptiles,
+                         int32_t* num_ptiles, int32_t* tile_cnt, int cnt_len, int* err,
+                         const LaunchOpts& o) {
   return launch(moe_align_kernel, dim3(chunks), dim3(kChunkAssign), 0, o, ids, chunk_hist, chunks,
-                A, E, chunk, offsets, sorted, inv, tiles, num_tiles, tile_cnt, cnt_len, err);
+                A, E, chunk, offsets, sorted, inv, tiles, num_tiles, ptiles, num_ptiles, tile_cnt,
+                cnt_len, err);
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted, int A, int k, int H,

@@ -63,7 +63,7 @@ class LevelStats(ctypes.Structure):
 class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "ids", "weights", "chunk_hist", "offsets", "sorted", "inv", "tiles", "num_tiles",
-        "x_sorted", "h", "y", "tile_cnt", "part", "total")] + [("chunks", ctypes.c_int32), ("max_tiles", ctypes.c_int32)]
+        "x_sorted", "h", "y", "ptiles", "num_ptiles", "tile_cnt", "part", "total")] + [("chunks", ctypes.c_int32), ("max_tiles", ctypes.c_int32)]
 
 
 class OffloadCounters(ctypes.Structure):

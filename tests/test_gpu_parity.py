@@ -238,3 +238,18 @@ def test_split_k_is_used_for_few_tiles_and_is_deterministic(oracle, make):
     check(a, w, run_oracle(oracle, w))
     for key in ("out", "h", "y"):
         assert np.array_equal(a[key], b[key]), key
+
+
+def test_paired_gemm1_with_odd_and_even_block_counts(oracle):
+    """1500 tokens of the tiny layer (3000 assignments, at least two 128-row blocks per
+    expert on average) take the GEMM 1 variant that pairs two row blocks of an expert per
+    CTA; a bias makes one expert hot (many blocks) and others small (a lone last block)."""
+    shape = wl.TINY
+    x = wl.make_x(17, 1500, shape.H)
+    bias = np.array([3.0, 0.0, -1.0, 0.5, -2.0, 1.0, 0.0, -0.5])
+    w = wl.build_simple("tiny_paired", shape, 1500, pool_pages=64, seed=17, x_bits=x,
+                        logits=wl.make_logits(17, x, shape.E, bias=bias))
+    o = run_oracle(oracle, w)
+    blocks = (np.diff(o["offsets"]) + 127) // 128
+    assert (blocks % 2 == 1).any() and (blocks % 2 == 0).any() and blocks.max() >= 4
+    check(run_gpu(w), w, o)
