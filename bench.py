@@ -28,6 +28,8 @@ sys.path.insert(0, ROOT)
 METRIC = "paged fused-MoE tokens/s; % of HBM / bf16 tensor roofline (Qwen3-30B-A3B)"
 DEFAULT_STEPS = {"q3_decode": 2000, "q3_prefill_zipf": 100, "q35_mixed_pool": 500, "tiny": 2000,
                  "q3_stack_offload": 32}
+REF_DEFAULT_STEPS = 20  # oracle steps when --impl reference is given no --steps
+REF_SECONDS = 120.0     # host time the oracle arm aims for, warm-up included
 WORKLOAD_TEXT = {
     "q3_decode": "Qwen3-30B-A3B-shaped MoE layer, decode: hidden 2048, moe intermediate 768, "
                  "128 experts, top-8 renormalised, 64 tokens; each w1/w3/w2 one 3 MiB page "
@@ -264,6 +266,16 @@ def run_offload(args, rank, world, local_rank):
     }
 
 
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time: the job has finished only when every replica has."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -344,10 +356,7 @@ def run_ours(args, rank, world, local_rank):
     dom_ms_live = ms_dom / max(n_dom, 1)
     if R.rimuru_get_device_error(ev) != R.DEV_OK:
         raise RuntimeError("device error in the timed region")
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / K
     value = world * w.T * K / (ms_total / 1e3)
 
@@ -374,10 +383,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     ms_e2e = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(ms_e2e, dist, dev)
     e2e_value = world * w.T * Ke / (ms_e2e / 1e3)
 
     # ---------------------------------------------------------------- roofline
@@ -480,7 +486,13 @@ def cpu_baseline(w, budget_s):
 def run_reference(args):
     import workloads as wl
     w = make_workload(args)
-    n, dt, cores = sample_tokens(w, budget_s=max(2.0, 120.0 / max(args.steps + args.warmup, 1)))
+    # every step is a sample of the workload's tokens, sized so that warm-up plus timed
+    # steps take about REF_SECONDS on the host cores (one token per step at the least)
+    per_step = REF_SECONDS / max(args.steps + args.warmup, 1)
+    n, dt, cores = sample_tokens(w, budget_s=4 * per_step)
+    while n > 1 and dt > per_step:
+        n = max(1, n // 2)
+        dt, cores = oracle_sample(w, np.arange(n))
     toks = np.arange(n)
     for _ in range(args.warmup):
         oracle_sample(w, toks)
@@ -522,7 +534,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = DEFAULT_STEPS[args.workload]
+        args.steps = REF_DEFAULT_STEPS if args.impl == "reference" else DEFAULT_STEPS[args.workload]
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
