@@ -291,6 +291,35 @@ int rimuru_moe_forward(const void* x_bf16, const float* logits, int num_tokens, 
                        void* stream);
 
 /*
+ * rimuru_moe_forward for activations that live in host memory.  The pages
+ * describe the layer on device-resident activations only; this entry point is
+ * the same layer with the copies in and out made part of the call.
+ * On `stream`, in order: x and logits are copied from the host buffers into
+ * device staging regions at the end of the workspace, the layer runs exactly as
+ * rimuru_moe_forward, and out is copied back to the host buffer.  The call
+ * returns once everything is queued; out_host is valid after the stream has
+ * been synchronised.
+ * Arguments:
+ *   x_host      host, bf16 [num_tokens][hidden]
+ *   logits_host host, fp32 [num_tokens][experts], finite
+ *   out_host    host, bf16 [num_tokens][hidden]
+ *   workspace   device, >= rimuru_moe_host_workspace_bytes(view, num_tokens)
+ *               bytes, 1024-byte aligned: the layer's workspace (same layout
+ *               as rimuru_moe_workspace_layout) followed by the staging copies
+ *               of x, logits and out
+ *   others      as rimuru_moe_forward
+ * Page-locked host buffers (cudaHostAlloc / cudaHostRegister) make the copies
+ * asynchronous; with pageable buffers the copy calls may block the host until
+ * they are done.  Host buffers must stay untouched until the stream is
+ * synchronised.  Errors as rimuru_moe_forward; RIMURU_ERR_CUDA if a copy cannot
+ * be queued.
+ */
+uint64_t rimuru_moe_host_workspace_bytes(rimuru_view_t view, int num_tokens);
+int rimuru_moe_forward_host(const void* x_host, const float* logits_host, int num_tokens,
+                            rimuru_view_t view, int layer, void* out_host, void* workspace,
+                            uint64_t workspace_bytes, void* stream);
+
+/*
  * The same layer as rimuru_moe_forward, for callers that cannot allocate
  * device memory.  The Rimuru pages have no counterpart of this entry point.
  *

@@ -89,6 +89,23 @@ void layout_for(const View& v, int T, rimuru_ws_layout* L) {
   L->max_tiles = static_cast<int32_t>(max_tiles);
 }
 
+// Device staging of the host-buffer forward, after the layer's own workspace.
+struct HostStaging {
+  uint64_t x, logits, out, total;
+};
+
+HostStaging host_staging(const View& v, int T) {
+  rimuru_ws_layout L;
+  layout_for(v, T, &L);
+  HostStaging s;
+  const uint64_t t = static_cast<uint64_t>(T);
+  s.x = align_up(L.total, 1024);
+  s.logits = align_up(s.x + t * v.hidden * 2, 1024);
+  s.out = align_up(s.logits + t * v.experts * 4, 1024);
+  s.total = align_up(s.out + t * v.hidden * 2, 1024);
+  return s;
+}
+
 }  // namespace
 
 int ensure_device_state(View* v) {
@@ -272,6 +289,50 @@ int rimuru_moe_forward(const void* x_bf16, const float* logits, int num_tokens, 
     d->prof_calls += 1;
   }
   return rimuru::launch_layer(a);
+}
+
+uint64_t rimuru_moe_host_workspace_bytes(rimuru_view_t view, int num_tokens) {
+  if (!view || !view->v.has_shape || num_tokens < 0) return 0;
+  return rimuru::host_staging(view->v, num_tokens).total;
+}
+
+int rimuru_moe_forward_host(const void* x_host, const float* logits_host, int num_tokens,
+                            rimuru_view_t view, int layer, void* out_host, void* workspace,
+                            uint64_t workspace_bytes, void* stream_ptr) {
+  rimuru::clear_error();
+  if (!view) return fail(RIMURU_ERR_ARG, "null view");
+  rimuru::View& v = view->v;
+  if (!v.has_shape) return fail(RIMURU_ERR_STATE, "view has no MoE shape");
+  if (num_tokens < 0 || num_tokens > (1 << 20))
+    return fail(RIMURU_ERR_ARG, "num_tokens must be in [0, 2^20]");
+  if (num_tokens > 0 && (!x_host || !logits_host || !out_host || !workspace))
+    return fail(RIMURU_ERR_ARG, "null pointer");
+  const rimuru::HostStaging s = rimuru::host_staging(v, num_tokens);
+  if (num_tokens > 0 && workspace_bytes < s.total)
+    return fail(RIMURU_ERR_WORKSPACE, "workspace needs " + std::to_string(s.total) + " bytes");
+  if (num_tokens > 0 && reinterpret_cast<uintptr_t>(workspace) % 1024 != 0)
+    return fail(RIMURU_ERR_ALIGN, "workspace must be 1024-byte aligned");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t xb = static_cast<size_t>(num_tokens) * v.hidden * 2;
+  const size_t lb = static_cast<size_t>(num_tokens) * v.experts * 4;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaError_t e = cudaSuccess;
+  // Checks that need no copy come first: an unmapped layer or a bad layer index
+  // is reported before anything is queued.
+  if (layer < 0 || layer >= v.layers) return fail(RIMURU_ERR_RANGE, "layer out of range");
+  if (v.mapped_per_layer[layer] != v.experts * 3)
+    return fail(RIMURU_ERR_UNMAPPED, "layer " + std::to_string(layer) + " has unmapped projections");
+  if (num_tokens == 0) return RIMURU_OK;
+  e = cudaMemcpyAsync(ws + s.x, x_host, xb, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ws + s.logits, logits_host, lb, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, rimuru::cuda_msg("input copy", e));
+  int st = rimuru_moe_forward(ws + s.x, reinterpret_cast<const float*>(ws + s.logits), num_tokens,
+                              view, layer, ws + s.out, workspace, s.x, stream_ptr);
+  if (st != RIMURU_OK) return st;
+  e = cudaMemcpyAsync(out_host, ws + s.out, xb, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, rimuru::cuda_msg("output copy", e));
+  return RIMURU_OK;
 }
 
 int rimuru_get_device_error(rimuru_view_t view, int* code, int clear) {

@@ -38,7 +38,7 @@ EXPORTS = [
     "rimuru_page_place", "rimuru_page_free", "rimuru_page_owned", "rimuru_view_set_moe_shape",
     "rimuru_expert_map", "rimuru_expert_unmap", "rimuru_expert_lookup",
     "rimuru_moe_workspace_bytes", "rimuru_moe_workspace_layout", "rimuru_moe_forward",
-    "rimuru_moe_forward_noalloc",
+    "rimuru_moe_forward_noalloc", "rimuru_moe_host_workspace_bytes", "rimuru_moe_forward_host",
     "rimuru_get_device_error", "rimuru_kernel_name", "rimuru_profile_enable",
     "rimuru_profile_read", "rimuru_device_sm_count", "rimuru_selftest_bounded_wait",
     "rimuru_offload_create", "rimuru_offload_destroy", "rimuru_offload_prefetch",
@@ -101,6 +101,8 @@ def _load():
         "rimuru_moe_workspace_layout": ([P, i32, ctypes.POINTER(WsLayout)], i32),
         "rimuru_moe_forward": ([P, P, i32, P, i32, P, P, u64, P], i32),
         "rimuru_moe_forward_noalloc": ([P, P, i32, P, i32, P, P, P], i32),
+        "rimuru_moe_host_workspace_bytes": ([P, i32], u64),
+        "rimuru_moe_forward_host": ([P, P, i32, P, i32, P, P, u64, P], i32),
         "rimuru_get_device_error": ([P, ctypes.POINTER(i32), i32], i32),
         "rimuru_kernel_name": ([i32], ctypes.c_char_p),
         "rimuru_profile_enable": ([P, i32, i32], i32),
@@ -256,6 +258,22 @@ def rimuru_moe_forward(x_ptr: int, logits_ptr: int, num_tokens: int, view, layer
                                   view, layer, ctypes.c_void_p(out_ptr),
                                   ctypes.c_void_p(workspace_ptr), workspace_bytes,
                                   ctypes.c_void_p(stream)))
+
+
+def rimuru_moe_host_workspace_bytes(view, num_tokens: int) -> int:
+    return int(lib.rimuru_moe_host_workspace_bytes(view, num_tokens))
+
+
+def rimuru_moe_forward_host(x_host_ptr: int, logits_host_ptr: int, num_tokens: int, view,
+                            layer: int, out_host_ptr: int, workspace_ptr: int,
+                            workspace_bytes: int, stream: int = 0) -> None:
+    """The forward on host buffers: x, logits and out are host addresses (page-locked for
+    asynchronous copies); the copies in and out run on ``stream`` with the layer."""
+    _check(lib.rimuru_moe_forward_host(ctypes.c_void_p(x_host_ptr),
+                                       ctypes.c_void_p(logits_host_ptr), num_tokens, view, layer,
+                                       ctypes.c_void_p(out_host_ptr),
+                                       ctypes.c_void_p(workspace_ptr), workspace_bytes,
+                                       ctypes.c_void_p(stream)))
 
 
 def rimuru_moe_forward_noalloc(x_ptr: int, logits_ptr: int, num_tokens: int, view, layer: int,

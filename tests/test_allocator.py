@@ -232,6 +232,42 @@ def test_forward_host_checks_run_before_any_device_work():
     R.rimuru_pool_destroy(pool)
 
 
+def test_host_buffer_forward_checks_and_staging_size():
+    """rimuru_moe_forward_host: the staging regions follow the layer's workspace, and bad
+    arguments are refused before any copy is queued."""
+    pool = R.rimuru_pool_create(FAKE_BASE, 32 * 64 * KiB, 64 * KiB)
+    ev = R.rimuru_view_create(pool, 64 * KiB)
+    R.rimuru_view_set_moe_shape(ev, 1, 8, 256, 128, 2)
+    fake = 1 << 30
+    T = 16
+    hws = R.rimuru_moe_host_workspace_bytes(ev, T)
+    ws = R.rimuru_moe_workspace_bytes(ev, T)
+    # x and out (T*H bf16) and logits (T*E fp32), each in its own 1 KiB-aligned region
+    assert hws >= ws + 2 * T * 256 * 2 + T * 8 * 4 and hws % 1024 == 0
+    assert R.rimuru_moe_host_workspace_bytes(ev, -1) == 0
+    with pytest.raises(R.RimuruError) as e:
+        R.rimuru_moe_forward_host(fake, fake, T, ev, 0, fake, fake, hws)
+    assert e.value.status == R.ERR_UNMAPPED
+    for ex in range(8):
+        for p in range(3):
+            R.rimuru_expert_map(ev, 0, ex, p, R.rimuru_page_alloc(ev))
+    with pytest.raises(R.RimuruError) as e:
+        R.rimuru_moe_forward_host(fake, fake, T, ev, 0, fake, fake, hws - 1)
+    assert e.value.status == R.ERR_WORKSPACE
+    with pytest.raises(R.RimuruError) as e:
+        R.rimuru_moe_forward_host(fake, fake, T, ev, 0, fake, fake + 512, hws)
+    assert e.value.status == R.ERR_ALIGN
+    with pytest.raises(R.RimuruError) as e:
+        R.rimuru_moe_forward_host(0, fake, T, ev, 0, fake, fake, hws)
+    assert e.value.status == R.ERR_ARG
+    with pytest.raises(R.RimuruError) as e:
+        R.rimuru_moe_forward_host(fake, fake, T, ev, 3, fake, fake, hws)
+    assert e.value.status == R.ERR_RANGE
+    R.rimuru_moe_forward_host(0, 0, 0, ev, 0, 0, 0, 0)   # zero tokens: nothing to do
+    R.rimuru_view_destroy(ev)
+    R.rimuru_pool_destroy(pool)
+
+
 def _kv_pool():
     pool = R.rimuru_pool_create(FAKE_BASE, 16 * 2 * MiB, 2 * MiB)
     ev = R.rimuru_view_create(pool, 2 * MiB)

@@ -253,3 +253,73 @@ def test_paired_gemm1_with_odd_and_even_block_counts(oracle):
     blocks = (np.diff(o["offsets"]) + 127) // 128
     assert (blocks % 2 == 1).any() and (blocks % 2 == 0).any() and blocks.max() >= 4
     check(run_gpu(w), w, o)
+
+
+# ------------------------------------------------- other sizes of the same layer family
+# Each case changes what the kernels tile over: a wider H and I (more k blocks and column
+# blocks), an I of 11 column blocks (odd, so GEMM 1 never pairs), H = 14 down-projection
+# tiles, 512 experts (the largest E the view accepts) with k = 10 (two combine groups), and
+# non-renormalised weights at the Qwen3.5-35B shape.
+SWEEP = {
+    "h4096_i1536_e32_k4_t64": (wl.MoEShape(H=4096, I=1536, E=32, k=4), 64, 16),
+    "h2048_i1408_e60_k4_t300": (wl.MoEShape(H=2048, I=1408, E=60, k=4), 300, 24),
+    "h3584_i2560_e16_k4_t40": (wl.MoEShape(H=3584, I=2560, E=16, k=4), 40, 12),
+    "h1024_i256_e512_k10_t64": (wl.MoEShape(H=1024, I=256, E=512, k=10), 64, None),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SWEEP))
+def test_layer_shape_sweep(oracle, name):
+    shape, T, n_sample = SWEEP[name]
+    w = wl.build_simple(name, shape, T, pool_pages=3 * shape.E + 16, seed=23)
+    tokens = None
+    if n_sample is not None:
+        tokens = np.sort(np.random.default_rng(23).choice(T, n_sample, replace=False))
+    check(run_gpu(w), w, run_oracle(oracle, w, tokens=tokens), tokens=tokens)
+
+
+def test_q35_mixed_pool_without_renormalisation(oracle):
+    """Top-8 of 256 experts with weights left as full-softmax probabilities."""
+    shape = wl.MoEShape(H=2048, I=512, E=256, k=8, renorm=False)
+    w = wl.build_mixed(shape, 256, seed=3)
+    o = run_oracle(oracle, w)
+    assert np.all(o["w"].sum(axis=1) < 1.0)
+    check(run_gpu(w), w, o)
+
+
+# ------------------------------------------------------------- host-buffer entry point
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_buffer_forward_equals_device_forward(oracle, pinned):
+    """rimuru_moe_forward_host copies x and logits in, runs the same launches and copies out
+    back: its output is bitwise the device-buffer forward's, and within the bar of the oracle."""
+    import torch
+
+    from paged_moe_shared_gb300 import rimuru as R
+
+    w = wl.tiny(5, T=300)
+    r = Runner(w)
+    try:
+        r.forward()
+        ref = r.results()
+        hws = R.rimuru_moe_host_workspace_bytes(r.ev, w.T)
+        raw = torch.empty(hws + 1024, dtype=torch.uint8, device="cuda:0")
+        ws = (raw.data_ptr() + 1023) // 1024 * 1024
+        hx = torch.from_numpy(w.x_bits.view(np.int16).copy())
+        hl = torch.from_numpy(np.ascontiguousarray(w.logits))
+        ho = torch.zeros(w.T, w.shape.H, dtype=torch.int16)
+        if pinned:
+            hx, hl, ho = hx.pin_memory(), hl.pin_memory(), ho.pin_memory()
+        s = torch.cuda.Stream()
+        for _ in range(2):  # the second call finds the first call's staging contents
+            R.rimuru_moe_forward_host(hx.data_ptr(), hl.data_ptr(), w.T, r.ev, 0, ho.data_ptr(),
+                                      ws, hws, s.cuda_stream)
+            s.synchronize()
+            assert R.rimuru_get_device_error(r.ev) == R.DEV_OK
+            assert torch.equal(ho, r.out.cpu().view(torch.int16))
+        # rows of the layer's own workspace hold the same intermediates as the device call
+        ids = raw[ws - raw.data_ptr():][r.layout["ids"]:r.layout["ids"] + w.T * w.shape.k * 4]
+        assert np.array_equal(ids.view(torch.int32).cpu().numpy().reshape(w.T, w.shape.k),
+                              ref["ids"])
+    finally:
+        r.close()
+    check(ref, w, run_oracle(oracle, w))
