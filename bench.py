@@ -500,7 +500,7 @@ def sample_tokens(w, budget_s):
 def cpu_baseline(w, budget_s):
     n, dt, cores = sample_tokens(w, budget_s)
     reps, total = 1, dt
-    while total < budget_s * 0.5 and reps < 8:
+    while total < budget_s * 0.5 and reps < 10000:
         d, _ = oracle_sample(w, np.arange(n))
         total += d
         reps += 1
