@@ -30,6 +30,7 @@ struct DeviceState {
   int prof_cap = 0;
   int prof_calls = 0;
   std::vector<cudaEvent_t> prof_ev;
+  std::vector<unsigned> prof_hits;  // per recorded forward: kernels that ran between their events
 };
 
 namespace {
@@ -286,6 +287,8 @@ int rimuru_moe_forward(const void* x_bf16, const float* logits, int num_tokens, 
   if (d->prof_on && d->prof_calls < d->prof_cap) {
     a.ev = &d->prof_ev[static_cast<size_t>(d->prof_calls) * RIMURU_K_COUNT * 2];
     a.ev_mask = d->prof_mask;
+    a.hits = &d->prof_hits[d->prof_calls];
+    *a.hits = 0u;
     d->prof_calls += 1;
   }
   return rimuru::launch_layer(a);
@@ -373,6 +376,7 @@ int rimuru_profile_enable(rimuru_view_t view, int kernel_mask, int capacity) {
     if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, rimuru::cuda_msg("cudaEventCreate", e));
     d->prof_ev.push_back(ev);
   }
+  d->prof_hits.assign(static_cast<size_t>(capacity), 0u);
   d->prof_cap = capacity;
   d->prof_calls = 0;
   d->prof_mask = static_cast<unsigned>(kernel_mask);
@@ -391,6 +395,7 @@ int rimuru_profile_read(rimuru_view_t view, int k, int* launches, double* total_
   rimuru::DeviceState* d = v.dev;
   if (!(d->prof_mask >> k & 1u)) return RIMURU_OK;
   for (int c = 0; c < d->prof_calls; ++c) {
+    if (!(d->prof_hits[c] >> k & 1u)) continue;  // kernel k is not part of this forward's path
     cudaEvent_t a = d->prof_ev[(static_cast<size_t>(c) * RIMURU_K_COUNT + k) * 2];
     cudaEvent_t b = d->prof_ev[(static_cast<size_t>(c) * RIMURU_K_COUNT + k) * 2 + 1];
     float ms = 0.f;

@@ -128,6 +128,7 @@ struct LayerLaunch {
   bool pdl = true;
   cudaEvent_t* ev = nullptr;        // 2 * RIMURU_K_COUNT events, or null
   unsigned ev_mask = 0;             // kernels bracketed by their event pair
+  unsigned* hits = nullptr;         // bit k set when kernel k was launched between its events
 };
 
 // Launch the six kernels of one layer.  Returns a rimuru status.

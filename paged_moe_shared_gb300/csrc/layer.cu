@@ -126,8 +126,10 @@ int launch_layer_route(const LayerLaunch& a) {
   next.pdl = a.pdl;
   cudaError_t e = cudaSuccess;
   auto mark = [&](int kidx, int which) {
-    if (a.ev && (a.ev_mask >> kidx & 1u) && e == cudaSuccess)
+    if (a.ev && (a.ev_mask >> kidx & 1u) && e == cudaSuccess) {
       e = cudaEventRecord(a.ev[kidx * 2 + which], a.stream);
+      if (which == 1 && a.hits) *a.hits |= 1u << kidx;
+    }
   };
   const int tpc = tokens_per_chunk(a.k);
   mark(RIMURU_K_ROUTE, 0);
@@ -198,8 +200,10 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route) {
   gather_o.pdl = after_route && a.pdl;  // directly behind align, or behind host-side work
   cudaError_t e = cudaSuccess;
   auto mark = [&](int kidx, int which) {
-    if (a.ev && (a.ev_mask >> kidx & 1u) && e == cudaSuccess)
+    if (a.ev && (a.ev_mask >> kidx & 1u) && e == cudaSuccess) {
       e = cudaEventRecord(a.ev[kidx * 2 + which], a.stream);
+      if (which == 1 && a.hits) *a.hits |= 1u << kidx;
+    }
   };
   mark(RIMURU_K_GATHER, 0);
   if (e == cudaSuccess)

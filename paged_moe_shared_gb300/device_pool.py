@@ -12,6 +12,7 @@ import torch
 from . import rimuru as R
 
 POOL_ALIGN = 2 << 20
+NAN_BITS = 0x7FC0  # bf16 quiet NaN: free pages read as NaN
 
 
 class DevicePool:
@@ -51,11 +52,13 @@ class DevicePool:
             pass
 
 
-def load_workload(w, device="cuda", layer: int = 0, layers: int = 1):
+def load_workload(w, device="cuda", layer: int = 0, layers: int = 1, extra_pages: int = 0):
     """Place a ``workloads.Workload`` in a new device pool: views first (expert view, then
     the KV view of a mixed pool), then every page through the allocator, then the bytes.
+    ``extra_pages`` adds free expert-view pages (NaN-filled) after the workload's pool.
     Returns (pool, expert_view, kv_view or None)."""
-    pool = DevicePool(w.pool_bytes, w.huge_page_bytes, device)
+    assert w.huge_page_bytes == w.page_bytes or extra_pages == 0
+    pool = DevicePool(w.pool_bytes + extra_pages * w.page_bytes, w.huge_page_bytes, device)
     ev = pool.view(w.page_bytes)
     kv = pool.view(w.kv_page_bytes) if w.kv_page_bytes else None
     s = w.shape
@@ -68,5 +71,23 @@ def load_workload(w, device="cuda", layer: int = 0, layers: int = 1):
     if kv is not None:
         for pid in w.kv_pages.tolist():
             R.rimuru_page_place(kv, int(pid))
-    pool.upload(w.pool)
+    if extra_pages:
+        pool.mem[:w.pool_bytes].copy_(torch.from_numpy(w.pool))
+        pool.mem[w.pool_bytes:].view(torch.int16).fill_(NAN_BITS)
+    else:
+        pool.upload(w.pool)
     return pool, ev, kv
+
+
+def replicate_layers(pool: DevicePool, ev, w, layers: int) -> None:
+    """Give layers 1 .. layers-1 their own copy of layer 0's expert pages: each projection is
+    copied on the device into a page taken from the allocator and mapped there, so every
+    layer holds the same weights at different addresses."""
+    pb = w.page_bytes
+    for layer in range(1, layers):
+        for e in range(w.shape.E):
+            for p in range(3):
+                src = int(w.page_table[e, p])
+                dst = R.rimuru_page_alloc(ev)
+                pool.mem[dst * pb:(dst + 1) * pb].copy_(pool.mem[src * pb:(src + 1) * pb])
+                R.rimuru_expert_map(ev, layer, e, p, dst)
