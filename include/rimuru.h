@@ -471,6 +471,10 @@ const char* rimuru_kernel_name(int k);
  * event pair between two kernels keeps the second from overlapping the
  * first, so bracket only the kernels being measured. */
 int rimuru_profile_enable(rimuru_view_t view, int kernel_mask, int capacity);
+/* The same, recording only every `every`-th forward (the first, then every
+ * `every` forwards after it) until `capacity` forwards are recorded, so that a
+ * long timed run is perturbed on a few of its forwards only.  every >= 1. */
+int rimuru_profile_enable_sampled(rimuru_view_t view, int kernel_mask, int capacity, int every);
 
 /* Launch count and summed device time (ms) of kernel slot `k` over the
  * recorded forwards (0 launches if `k` was not selected).  Synchronises on

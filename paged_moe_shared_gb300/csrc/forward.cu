@@ -29,6 +29,8 @@ struct DeviceState {
   unsigned prof_mask = 0;  // kernels bracketed by an event pair
   int prof_cap = 0;
   int prof_calls = 0;
+  int prof_every = 1;   // record every prof_every-th forward
+  long long prof_seen = 0;  // forwards since profiling was enabled
   std::vector<cudaEvent_t> prof_ev;
   std::vector<unsigned> prof_hits;  // per recorded forward: kernels that ran between their events
 };
@@ -284,7 +286,7 @@ int rimuru_moe_forward(const void* x_bf16, const float* logits, int num_tokens, 
   a.stream = stream;
   a.sm_count = rimuru::sm_count_of(d->device);
   if (a.sm_count <= 0) return fail(RIMURU_ERR_CUDA, "could not query the SM count");
-  if (d->prof_on && d->prof_calls < d->prof_cap) {
+  if (d->prof_on && d->prof_calls < d->prof_cap && d->prof_seen++ % d->prof_every == 0) {
     a.ev = &d->prof_ev[static_cast<size_t>(d->prof_calls) * RIMURU_K_COUNT * 2];
     a.ev_mask = d->prof_mask;
     a.hits = &d->prof_hits[d->prof_calls];
@@ -355,7 +357,12 @@ int rimuru_get_device_error(rimuru_view_t view, int* code, int clear) {
 }
 
 int rimuru_profile_enable(rimuru_view_t view, int kernel_mask, int capacity) {
+  return rimuru_profile_enable_sampled(view, kernel_mask, capacity, 1);
+}
+
+int rimuru_profile_enable_sampled(rimuru_view_t view, int kernel_mask, int capacity, int every) {
   rimuru::clear_error();
+  if (every < 1) return fail(RIMURU_ERR_ARG, "every must be >= 1");
   if (!view) return fail(RIMURU_ERR_ARG, "null view");
   rimuru::View& v = view->v;
   if (!v.has_shape) return fail(RIMURU_ERR_STATE, "view has no MoE shape");
@@ -379,6 +386,8 @@ int rimuru_profile_enable(rimuru_view_t view, int kernel_mask, int capacity) {
   d->prof_hits.assign(static_cast<size_t>(capacity), 0u);
   d->prof_cap = capacity;
   d->prof_calls = 0;
+  d->prof_every = every;
+  d->prof_seen = 0;
   d->prof_mask = static_cast<unsigned>(kernel_mask);
   d->prof_on = true;
   return RIMURU_OK;

@@ -40,6 +40,7 @@ EXPORTS = [
     "rimuru_moe_workspace_bytes", "rimuru_moe_workspace_layout", "rimuru_moe_forward",
     "rimuru_moe_forward_noalloc", "rimuru_moe_host_workspace_bytes", "rimuru_moe_forward_host",
     "rimuru_get_device_error", "rimuru_kernel_name", "rimuru_profile_enable",
+    "rimuru_profile_enable_sampled",
     "rimuru_profile_read", "rimuru_device_sm_count", "rimuru_selftest_bounded_wait",
     "rimuru_offload_create", "rimuru_offload_destroy", "rimuru_offload_prefetch",
     "rimuru_offload_forward", "rimuru_offload_stats", "rimuru_offload_resident",
@@ -106,6 +107,7 @@ def _load():
         "rimuru_get_device_error": ([P, ctypes.POINTER(i32), i32], i32),
         "rimuru_kernel_name": ([i32], ctypes.c_char_p),
         "rimuru_profile_enable": ([P, i32, i32], i32),
+        "rimuru_profile_enable_sampled": ([P, i32, i32, i32], i32),
         "rimuru_profile_read": ([P, i32, ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_double)], i32),
         "rimuru_device_sm_count": ([], i32),
         "rimuru_selftest_bounded_wait": ([ctypes.c_uint32, ctypes.POINTER(i32)], i32),
@@ -304,6 +306,11 @@ PROFILE_ALL = (1 << K_COUNT) - 1
 def rimuru_profile_enable(view, kernel_mask: int, capacity: int = 1024) -> None:
     """Bracket the kernels in ``kernel_mask`` (bit K_*) with CUDA events; 0 stops."""
     _check(lib.rimuru_profile_enable(view, int(kernel_mask), capacity))
+
+
+def rimuru_profile_enable_sampled(view, kernel_mask: int, capacity: int, every: int) -> None:
+    """Event pairs around the selected kernels of every ``every``-th forward only."""
+    _check(lib.rimuru_profile_enable_sampled(view, int(kernel_mask), capacity, every))
 
 
 def rimuru_profile_read(view, k: int):

@@ -264,6 +264,9 @@ def test_host_buffer_forward_checks_and_staging_size():
         R.rimuru_moe_forward_host(fake, fake, T, ev, 3, fake, fake, hws)
     assert e.value.status == R.ERR_RANGE
     R.rimuru_moe_forward_host(0, 0, 0, ev, 0, 0, 0, 0)   # zero tokens: nothing to do
+    with pytest.raises(R.RimuruError) as e:              # sampling stride must be >= 1
+        R.rimuru_profile_enable_sampled(ev, 1, 10, 0)
+    assert e.value.status == R.ERR_ARG
     R.rimuru_view_destroy(ev)
     R.rimuru_pool_destroy(pool)
 
