@@ -451,7 +451,11 @@ int rimuru_get_device_error(rimuru_view_t view, int* code, int clear);
 
 /* ------------------------------------------------------------- profiling */
 
-/* Kernels launched by one forward, in launch order. */
+/* Kernel slots of one forward.  A forward launches route, align, gather,
+ * GEMM 1, GEMM 2, combine in that order, except when its T * top_k
+ * assignments fit one CTA (at most 1024): then one kernel in slot
+ * RIMURU_K_ROUTE_ALIGN_GATHER does the first three steps, followed by GEMM 1,
+ * GEMM 2 and combine. */
 enum {
   RIMURU_K_ROUTE = 0,
   RIMURU_K_ALIGN = 1,
@@ -459,7 +463,8 @@ enum {
   RIMURU_K_GEMM1 = 3,
   RIMURU_K_GEMM2 = 4,
   RIMURU_K_COMBINE = 5,
-  RIMURU_K_COUNT = 6
+  RIMURU_K_ROUTE_ALIGN_GATHER = 6,
+  RIMURU_K_COUNT = 7
 };
 
 /* Name of kernel slot `k` ("moe_route", ...), or NULL. */

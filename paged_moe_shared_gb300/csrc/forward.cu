@@ -227,8 +227,9 @@ int rimuru_device_sm_count(void) {
 }
 
 const char* rimuru_kernel_name(int k) {
-  static const char* names[RIMURU_K_COUNT] = {"moe_route", "moe_align", "moe_gather",
-                                              "moe_gemm1_swiglu", "moe_gemm2", "moe_combine"};
+  static const char* names[RIMURU_K_COUNT] = {"moe_route",        "moe_align", "moe_gather",
+                                              "moe_gemm1_swiglu", "moe_gemm2", "moe_combine",
+                                              "moe_route_align_gather"};
   return (k >= 0 && k < RIMURU_K_COUNT) ? names[k] : nullptr;
 }
 

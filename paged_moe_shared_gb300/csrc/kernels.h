@@ -60,6 +60,18 @@ cudaError_t launch_align(const int32_t* ids, const int32_t* chunk_hist, int chun
                          int32_t* num_ptiles, int32_t* tile_cnt, int cnt_len, int* err,
                          const LaunchOpts& o);
 
+// a1 + a2 + gather in one launch for batches whose A = T * k assignments fit
+// one CTA (A <= kChunkAssign): every CTA routes and groups all assignments in
+// shared memory, CTA 0 writes the tables, each CTA gathers its share of rows
+// (about kFusedRowsPerCta of them).
+constexpr int kFusedRowsPerCta = 8;
+cudaError_t launch_route_align_gather(const float* logits, const __nv_bfloat16* x, int T, int E,
+                                      int k, int renorm, int H, int32_t* ids, float* w,
+                                      int32_t* offsets, int32_t* sorted, int32_t* inv,
+                                      int32_t* tiles, int32_t* num_tiles, int32_t* ptiles,
+                                      int32_t* num_ptiles, int32_t* tile_cnt, int cnt_len,
+                                      __nv_bfloat16* x_sorted, int* err, const LaunchOpts& o);
+
 // x rows in expert-sorted order: x_sorted[r] = x[sorted[r] / k].
 cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted, int A, int k, int H,
                           __nv_bfloat16* x_sorted, const LaunchOpts& o);
@@ -137,6 +149,7 @@ int launch_layer(const LayerLaunch& a);
 // GEMM 1, GEMM 2, combine).  Host-side work may sit between the two;
 // after_route = false when it does (the gather then follows it in stream order).
 int launch_layer_route(const LayerLaunch& a);
-int launch_layer_experts(const LayerLaunch& a, bool after_route);
+// gathered = true when x_sorted is already written (the small-batch kernel).
+int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered = false);
 
 }  // namespace rimuru

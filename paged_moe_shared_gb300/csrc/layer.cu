@@ -146,7 +146,7 @@ int launch_layer_route(const LayerLaunch& a) {
   return RIMURU_OK;
 }
 
-int launch_layer_experts(const LayerLaunch& a, bool after_route) {
+int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) {
   const rimuru_ws_layout& L = a.layout;
   const LayerPtrs q = pointers_of(a);
   const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I;
@@ -205,10 +205,12 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route) {
       if (which == 1 && a.hits) *a.hits |= 1u << kidx;
     }
   };
-  mark(RIMURU_K_GATHER, 0);
-  if (e == cudaSuccess)
-    e = launch_gather(static_cast<const __nv_bfloat16*>(a.x), q.sorted, A, k, H, q.xs, gather_o);
-  mark(RIMURU_K_GATHER, 1);
+  if (!gathered) {
+    mark(RIMURU_K_GATHER, 0);
+    if (e == cudaSuccess)
+      e = launch_gather(static_cast<const __nv_bfloat16*>(a.x), q.sorted, A, k, H, q.xs, gather_o);
+    mark(RIMURU_K_GATHER, 1);
+  }
   mark(RIMURU_K_GEMM1, 0);
   const bool paired = sp.s1 == 1 &&
                       static_cast<long long>(A) >= static_cast<long long>(kPairMinBlocksPerExpert) * kTileM * E;
@@ -235,9 +237,32 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route) {
 }
 
 int launch_layer(const LayerLaunch& a) {
-  int st = launch_layer_route(a);
-  if (st != RIMURU_OK) return st;
-  return launch_layer_experts(a, /*after_route=*/true);
+  if (static_cast<long long>(a.T) * a.k > kChunkAssign) {
+    int st = launch_layer_route(a);
+    if (st != RIMURU_OK) return st;
+    return launch_layer_experts(a, /*after_route=*/true, /*gathered=*/false);
+  }
+  // small batch: route, align and gather in one kernel
+  const LayerPtrs q = pointers_of(a);
+  LaunchOpts first;
+  first.stream = a.stream;
+  first.sm_count = a.sm_count;
+  first.pdl = false;  // the first kernel follows whatever the caller queued
+  cudaError_t e = cudaSuccess;
+  const int kidx = RIMURU_K_ROUTE_ALIGN_GATHER;
+  const bool prof = a.ev && (a.ev_mask >> kidx & 1u);
+  if (prof) e = cudaEventRecord(a.ev[kidx * 2], a.stream);
+  if (e == cudaSuccess)
+    e = launch_route_align_gather(
+        a.logits, static_cast<const __nv_bfloat16*>(a.x), a.T, a.E, a.k, a.renorm, a.H, q.ids, q.w,
+        q.offsets, q.sorted, q.inv, q.tiles, q.num_tiles, q.ptiles, q.num_ptiles, q.tile_cnt,
+        static_cast<int>(2 * std::max(splits_of(a).t1, splits_of(a).t2)), q.xs, a.err, first);
+  if (prof && e == cudaSuccess) {
+    e = cudaEventRecord(a.ev[kidx * 2 + 1], a.stream);
+    if (a.hits) *a.hits |= 1u << kidx;
+  }
+  if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, cuda_msg("kernel launch", e));
+  return launch_layer_experts(a, /*after_route=*/true, /*gathered=*/true);
 }
 
 }  // namespace rimuru

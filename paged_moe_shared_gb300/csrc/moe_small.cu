@@ -46,10 +46,70 @@ __device__ __forceinline__ float key_value(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
-// One warp per token.  Lane l holds experts l, l + 32, ... (EPL per lane) as
-// keys; each of the k rounds takes the largest untaken key of the warp with
-// one redux.max and, among lanes holding it, the lowest expert index with one
-// redux.min.  Key 0 marks lanes past E (valid keys are >= key(-inf) > 0).
+// Routing of one token by one warp.  Lane l holds experts l, l + 32, ...
+// (EPL per lane) as keys; each of the k rounds takes the largest untaken key
+// of the warp with one redux.max and, among lanes holding it, the lowest
+// expert index with one redux.min.  Key 0 marks lanes past E (valid keys are
+// >= key(-inf) > 0).  Lane j < k receives slot j: its expert and weight.
+template <int EPL>
+__device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k,
+                                            int renorm, int lane, int* err, int& my_id,
+                                            float& my_w) {
+  uint32_t key[EPL];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = 0u;
+    if (e < E) {
+      float x = row[e];
+      if (!isfinite(x)) {
+        bad = true;
+        x = -INFINITY;  // invalid input: rank it last, keep ids valid
+      }
+      key[i] = order_key(x);
+    }
+  }
+  if (__any_sync(kFull, bad) && lane == 0) set_error(err, RIMURU_DEV_NONFINITE);
+  uint32_t taken = 0;
+  float mx = 0.f, psum = 0.f, my_p = 0.f;
+  my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0u, bi = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      if (!((taken >> i) & 1u) && key[i] > bk) {  // strict: lowest index among equals
+        bk = key[i];
+        bi = static_cast<uint32_t>(lane + 32 * i);
+      }
+    }
+    const uint32_t m = __reduce_max_sync(kFull, bk);
+    const uint32_t win = __reduce_min_sync(kFull, bk == m ? bi : 0xffffffffu);
+    const float v = key_value(m);
+    if (j == 0) mx = (v == -INFINITY) ? 0.f : v;  // largest logit of the token
+    if (static_cast<int>(win & 31u) == lane) taken |= 1u << (win >> 5);
+    const float p = expf(v - mx);
+    psum += p;
+    if (lane == j) {
+      my_id = static_cast<int>(win);
+      my_p = p;
+    }
+  }
+  float denom = psum;
+  if (!renorm) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (key[i] != 0u) s += expf(key_value(key[i]) - mx);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+    denom = s;
+  }
+  my_w = my_p / denom;
+}
+
+// One warp per token over the chunk's tokens; the chunk's expert histogram
+// goes to chunk_hist[blockIdx.x].
 template <int EPL>
 __global__ void __launch_bounds__(1024) moe_route_kernel(const float* __restrict__ logits, int T,
                                                          int E, int k, int renorm, int tpc,
@@ -67,60 +127,12 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const float* __restrict
   const int t_begin = blockIdx.x * tpc;
   const int t_end = min(t_begin + tpc, T);
   for (int t = t_begin + warp; t < t_end; t += nwarps) {
-    const float* row = logits + static_cast<size_t>(t) * E;
-    uint32_t key[EPL];
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      key[i] = 0u;
-      if (e < E) {
-        float x = row[e];
-        if (!isfinite(x)) {
-          bad = true;
-          x = -INFINITY;  // invalid input: rank it last, keep ids valid
-        }
-        key[i] = order_key(x);
-      }
-    }
-    if (__any_sync(kFull, bad) && lane == 0) set_error(err, RIMURU_DEV_NONFINITE);
-    uint32_t taken = 0;
-    float mx = 0.f, psum = 0.f, my_p = 0.f;
-    int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-      uint32_t bk = 0u, bi = 0xffffffffu;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        if (!((taken >> i) & 1u) && key[i] > bk) {  // strict: lowest index among equals
-          bk = key[i];
-          bi = static_cast<uint32_t>(lane + 32 * i);
-        }
-      }
-      const uint32_t m = __reduce_max_sync(kFull, bk);
-      const uint32_t win = __reduce_min_sync(kFull, bk == m ? bi : 0xffffffffu);
-      const float v = key_value(m);
-      if (j == 0) mx = (v == -INFINITY) ? 0.f : v;  // largest logit of the token
-      if (static_cast<int>(win & 31u) == lane) taken |= 1u << (win >> 5);
-      const float p = expf(v - mx);
-      psum += p;
-      if (lane == j) {
-        my_id = static_cast<int>(win);
-        my_p = p;
-      }
-    }
-    float denom = psum;
-    if (!renorm) {
-      float s = 0.f;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (key[i] != 0u) s += expf(key_value(key[i]) - mx);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
-      denom = s;
-    }
+    int my_id;
+    float my_w;
+    route_token<EPL>(logits + static_cast<size_t>(t) * E, E, k, renorm, lane, err, my_id, my_w);
     if (lane < k) {
       ids[static_cast<size_t>(t) * k + lane] = my_id;
-      w[static_cast<size_t>(t) * k + lane] = my_p / denom;
+      w[static_cast<size_t>(t) * k + lane] = my_w;
       atomicAdd(&s_hist[my_id], 1);
     }
   }
@@ -154,6 +166,33 @@ __device__ int block_exclusive_scan(int v, int* s_warp) {
   int before = warp > 0 ? s_warp[warp - 1] : 0;
   __syncthreads();  // s_warp may be reused by the caller
   return before + x - v;
+}
+
+// Offsets, the 128-row tile table, the table of 256-row pairs of blocks and the
+// zeroed split-K counters, from each expert's count `tot` and exclusive offset
+// `off` (held by thread e of the CTA for e < E).  Every thread of the CTA calls it.
+__device__ void write_tables(int E, int tot, int off, int32_t* __restrict__ offsets,
+                             int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles,
+                             int32_t* __restrict__ ptiles, int32_t* __restrict__ num_ptiles,
+                             int32_t* __restrict__ tile_cnt, int cnt_len, int* s_warp) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < cnt_len; i += blockDim.x) tile_cnt[i] = 0;
+  if (tid < E) offsets[tid] = off;
+  if (tid == E - 1) offsets[E] = off + tot;
+  const int nb = tid < E ? (tot + kTileM - 1) / kTileM : 0;
+  const int first = block_exclusive_scan(nb, s_warp);
+  for (int b = 0; b < nb; ++b) {
+    tiles[2 * (first + b)] = tid;
+    tiles[2 * (first + b) + 1] = off + b * kTileM;
+  }
+  if (tid == E - 1) *num_tiles = first + nb;
+  const int np = (nb + 1) / 2;  // pairs of blocks, the last one possibly alone
+  const int pfirst = block_exclusive_scan(np, s_warp);
+  for (int b = 0; b < np; ++b) {
+    ptiles[2 * (pfirst + b)] = tid;
+    ptiles[2 * (pfirst + b) + 1] = off + b * 2 * kTileM;
+  }
+  if (tid == E - 1) *num_ptiles = pfirst + np;
 }
 
 // ----------------------------------------------------------------- align
@@ -205,29 +244,9 @@ __global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
   }
   const int off = block_exclusive_scan(tot, s_warp);
   if (tid < E) s_base[tid] = off + before;
-  if (c == 0) {
-    for (int i = tid; i < cnt_len; i += blockDim.x) tile_cnt[i] = 0;
-    if (tid < E) offsets[tid] = off;
-    if (tid == E - 1) offsets[E] = off + tot;
-    const int nb = (tot + kTileM - 1) / kTileM;
-    const int first = block_exclusive_scan(nb, s_warp);
-    if (tid < E) {
-      for (int b = 0; b < nb; ++b) {
-        tiles[2 * (first + b)] = tid;
-        tiles[2 * (first + b) + 1] = off + b * kTileM;
-      }
-    }
-    if (tid == E - 1) *num_tiles = first + nb;
-    const int np = (nb + 1) / 2;  // pairs of blocks, the last one possibly alone
-    const int pfirst = block_exclusive_scan(np, s_warp);
-    if (tid < E) {
-      for (int b = 0; b < np; ++b) {
-        ptiles[2 * (pfirst + b)] = tid;
-        ptiles[2 * (pfirst + b) + 1] = off + b * 2 * kTileM;
-      }
-    }
-    if (tid == E - 1) *num_ptiles = pfirst + np;
-  }
+  if (c == 0)
+    write_tables(E, tot, off, offsets, tiles, num_tiles, ptiles, num_ptiles, tile_cnt, cnt_len,
+                 s_warp);
   __syncthreads();
   if (tid < n) {
     const int my = s_ids[tid];
@@ -265,6 +284,106 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict
 #pragma unroll
       for (int i = 0; i < kGatherRows; ++i)
         if (t[i] >= 0) xs[static_cast<size_t>(r0 + i) * H8 + c] = v[i];
+    }
+  }
+}
+
+// ----------------------------------------------------- small batches, one launch
+// Route, align and gather in one kernel when all A = T * k assignments fit one
+// CTA (A <= kChunkAssign, decode-sized batches).  Every CTA routes all T tokens
+// and groups the assignments in shared memory: a few microseconds of repeated
+// work per CTA instead of two kernel boundaries and the global round trip of
+// the routing tables.  CTA 0 writes ids, weights, offsets, sorted, inv and the
+// tile tables; every CTA copies its share of the rows into x_sorted.
+// Grouping: assignment f = 32 g + lane belongs to warp g; within the warp its
+// rank among equal experts comes from __match_any_sync, across warps from a
+// prefix over per-warp counts, so the order is f ascending inside each expert.
+constexpr int kFusedWarps = kChunkAssign / 32;
+
+template <int EPL>
+__global__ void __launch_bounds__(kChunkAssign) moe_route_align_gather_kernel(
+    const float* __restrict__ logits, const uint4* __restrict__ x, int T, int E, int k,
+    int renorm, int H8, int32_t* __restrict__ ids, float* __restrict__ w,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted, int32_t* __restrict__ inv,
+    int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles, int32_t* __restrict__ ptiles,
+    int32_t* __restrict__ num_ptiles, int32_t* __restrict__ tile_cnt, int cnt_len,
+    uint4* __restrict__ xs, int* err) {
+  __shared__ int s_ids[kChunkAssign];                     // expert of assignment f
+  __shared__ int s_sorted[kChunkAssign];                  // assignment held by sorted row r
+  __shared__ uint16_t s_wh[kFusedWarps][kMaxExperts];     // per-warp counts, then their prefix
+  __shared__ int s_off[kMaxExperts];
+  __shared__ int s_warp[32];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int A = T * k;
+  const int groups = (A + 31) / 32;
+  const bool lead = blockIdx.x == 0;
+  for (int i = tid; i < groups * kMaxExperts; i += blockDim.x) (&s_wh[0][0])[i] = 0;
+  for (int t = warp; t < T; t += kFusedWarps) {
+    int my_id;
+    float my_w;
+    route_token<EPL>(logits + static_cast<size_t>(t) * E, E, k, renorm, lane, err, my_id, my_w);
+    if (lane < k) {
+      s_ids[t * k + lane] = my_id;
+      if (lead) {
+        ids[t * k + lane] = my_id;
+        w[t * k + lane] = my_w;
+      }
+    }
+  }
+  __syncthreads();
+  const int f = warp * 32 + lane;
+  const unsigned valid = __ballot_sync(kFull, f < A);
+  int my_e = 0, rank_in = 0;
+  if (f < A) {
+    my_e = s_ids[f];
+    const unsigned peers = __match_any_sync(valid, my_e);
+    rank_in = __popc(peers & ((1u << lane) - 1u));
+    if (rank_in == 0) s_wh[warp][my_e] = static_cast<uint16_t>(__popc(peers));
+  }
+  __syncthreads();
+  int tot = 0;
+  if (tid < E) {
+    for (int g = 0; g < groups; ++g) {
+      const int v = s_wh[g][tid];
+      s_wh[g][tid] = static_cast<uint16_t>(tot);
+      tot += v;
+    }
+  }
+  const int off = block_exclusive_scan(tot, s_warp);
+  if (tid < E) s_off[tid] = off;
+  if (lead)
+    write_tables(E, tot, off, offsets, tiles, num_tiles, ptiles, num_ptiles, tile_cnt, cnt_len,
+                 s_warp);
+  __syncthreads();
+  if (f < A) {
+    const int pos = s_off[my_e] + s_wh[warp][my_e] + rank_in;
+    s_sorted[pos] = f;
+    if (lead) {
+      sorted[pos] = f;
+      inv[f] = pos;
+    }
+  }
+  __syncthreads();
+  // this CTA's rows of x_sorted, four 16-byte loads in flight per thread
+  const int per = (A + gridDim.x - 1) / gridDim.x;
+  const int r0 = min(A, blockIdx.x * per), r1 = min(A, r0 + per);
+  const int n = (r1 - r0) * H8;
+  for (int i0 = tid; i0 < n; i0 += 4 * blockDim.x) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n) {
+        const int r = r0 + i / H8, c = i % H8;
+        v[u] = x[static_cast<size_t>(s_sorted[r] / k) * H8 + c];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n) xs[static_cast<size_t>(r0) * H8 + i] = v[u];
     }
   }
 }
@@ -356,6 +475,34 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted, int A, 
   const int grid = min(blocks, o.sm_count * 8);
   return launch(moe_gather_kernel, dim3(grid), dim3(256), 0, o, reinterpret_cast<const uint4*>(x),
                 sorted, A, k, H / 8, reinterpret_cast<uint4*>(x_sorted));
+}
+
+cudaError_t launch_route_align_gather(const float* logits, const __nv_bfloat16* x, int T, int E,
+                                      int k, int renorm, int H, int32_t* ids, float* w,
+                                      int32_t* offsets, int32_t* sorted, int32_t* inv,
+                                      int32_t* tiles, int32_t* num_tiles, int32_t* ptiles,
+                                      int32_t* num_ptiles, int32_t* tile_cnt, int cnt_len,
+                                      __nv_bfloat16* x_sorted, int* err, const LaunchOpts& o) {
+  const int A = T * k;
+  const int grid = max(1, min((A + kFusedRowsPerCta - 1) / kFusedRowsPerCta, o.sm_count));
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  uint4* xsv = reinterpret_cast<uint4*>(x_sorted);
+  const dim3 g(grid), b(kChunkAssign);
+  if (E <= 32)
+    return launch(moe_route_align_gather_kernel<1>, g, b, 0, o, logits, xv, T, E, k, renorm, H / 8,
+                  ids, w, offsets, sorted, inv, tiles, num_tiles, ptiles, num_ptiles, tile_cnt,
+                  cnt_len, xsv, err);
+  if (E <= 128)
+    return launch(moe_route_align_gather_kernel<4>, g, b, 0, o, logits, xv, T, E, k, renorm, H / 8,
+                  ids, w, offsets, sorted, inv, tiles, num_tiles, ptiles, num_ptiles, tile_cnt,
+                  cnt_len, xsv, err);
+  if (E <= 256)
+    return launch(moe_route_align_gather_kernel<8>, g, b, 0, o, logits, xv, T, E, k, renorm, H / 8,
+                  ids, w, offsets, sorted, inv, tiles, num_tiles, ptiles, num_ptiles, tile_cnt,
+                  cnt_len, xsv, err);
+  return launch(moe_route_align_gather_kernel<16>, g, b, 0, o, logits, xv, T, E, k, renorm, H / 8,
+                ids, w, offsets, sorted, inv, tiles, num_tiles, ptiles, num_ptiles, tile_cnt,
+                cnt_len, xsv, err);
 }
 
 cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv, const float* w, int T,

@@ -28,7 +28,7 @@ ERR_UNSUPPORTED = -10
 PROJ_W1, PROJ_W3, PROJ_W2 = 0, 1, 2
 NEW_GROUP = -2
 DEV_OK, DEV_BAD_PAGE, DEV_NONFINITE, DEV_TIMEOUT, DEV_BAD_SHAPE = 0, 1, 2, 3, 4
-K_ROUTE, K_ALIGN, K_GATHER, K_GEMM1, K_GEMM2, K_COMBINE, K_COUNT = range(7)
+K_ROUTE, K_ALIGN, K_GATHER, K_GEMM1, K_GEMM2, K_COMBINE, K_ROUTE_ALIGN_GATHER, K_COUNT = range(8)
 
 # Every symbol include/rimuru.h declares.
 EXPORTS = [

@@ -82,6 +82,33 @@ def test_tiny_ragged_token_counts(oracle, T):
     check(run_gpu(w), w, run_oracle(oracle, w))
 
 
+@pytest.mark.parametrize("T,fused", [(512, True), (513, False)])
+def test_small_batch_kernel_boundary(oracle, T, fused):
+    """Up to 1024 assignments (T * k) route, align and gather in one kernel; one more takes
+    the three-kernel path.  Both sides of the boundary against the oracle, and the kernels
+    each side launched, read from the library's per-kernel profile."""
+    from paged_moe_shared_gb300 import rimuru as R
+
+    w = wl.tiny(8, T=T)
+    r = Runner(w)
+    try:
+        R.rimuru_profile_enable(r.ev, R.PROFILE_ALL, 1)
+        r.forward()
+        res = r.results()
+        launched = {R.rimuru_kernel_name(i): R.rimuru_profile_read(r.ev, i)[0]
+                    for i in range(R.K_COUNT)}
+        R.rimuru_profile_enable(r.ev, 0, 1)
+    finally:
+        r.close()
+    small = {"moe_route_align_gather": 1, "moe_route": 0, "moe_align": 0, "moe_gather": 0}
+    large = {"moe_route_align_gather": 0, "moe_route": 1, "moe_align": 1, "moe_gather": 1}
+    for name, n in (small if fused else large).items():
+        assert launched[name] == n, (name, launched)
+    for name in ("moe_gemm1_swiglu", "moe_gemm2", "moe_combine"):
+        assert launched[name] == 1
+    check(res, w, run_oracle(oracle, w))
+
+
 @pytest.mark.parametrize("k", [1, 3, 8])
 def test_tiny_top_k(oracle, k):
     """k = 1 (argmax expert), k = 3, and k = E = 8 (every expert, dense mixture)."""
