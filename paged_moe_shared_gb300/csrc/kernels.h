@@ -98,13 +98,17 @@ struct GemmArgs {
 // a3: h = silu(x_sorted w1_e) * (x_sorted w3_e); w1/w3 read in place from pages.
 cudaError_t launch_gemm1_swiglu(const CUtensorMap& tm_x, const CUtensorMap& tm_w13,
                                 const GemmArgs& a, const LaunchOpts& o);
-// a3 for large batches: the same GEMM with two row blocks of an expert per CTA
-// sharing each weight tile (tiles/num_tiles in `a` name the pair table).
-cudaError_t launch_gemm1_swiglu_paired(const CUtensorMap& tm_x, const CUtensorMap& tm_w13,
-                                       const GemmArgs& a, const LaunchOpts& o);
-// Use the paired GEMM 1 when the assignments average at least this many
+// Use the CTA-pair GEMMs when the assignments average at least this many
 // 128-row blocks per expert (most experts then have pairs of blocks).
 constexpr int kPairMinBlocksPerExpert = 2;
+
+// a3 and a4 for large batches on CTA pairs (tcgen05 cta_group::2): a tile is
+// one entry of the pair table (tiles/num_tiles in `a` name it) times one
+// column block; each CTA stages half of every weight tile.
+cudaError_t launch_gemm1_swiglu_pair(const CUtensorMap& tm_x, const CUtensorMap& tm_w13,
+                                     const GemmArgs& a, const LaunchOpts& o);
+cudaError_t launch_gemm2_pair(const CUtensorMap& tm_h, const CUtensorMap& tm_w2, const GemmArgs& a,
+                              const LaunchOpts& o);
 
 // a4: y = h w2_e; w2 read in place from its page.
 cudaError_t launch_gemm2(const CUtensorMap& tm_h, const CUtensorMap& tm_w2, const GemmArgs& a,

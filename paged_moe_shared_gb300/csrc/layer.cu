@@ -212,21 +212,27 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
     mark(RIMURU_K_GATHER, 1);
   }
   mark(RIMURU_K_GEMM1, 0);
-  const bool paired = sp.s1 == 1 &&
-                      static_cast<long long>(A) >= static_cast<long long>(kPairMinBlocksPerExpert) * kTileM * E;
+  // Large batches (at least two 128-row blocks per expert on average) run both
+  // GEMMs on CTA pairs over the table of 256-row pairs of blocks.
+  const bool pairs = static_cast<long long>(A) >=
+                     static_cast<long long>(kPairMinBlocksPerExpert) * kTileM * E;
+  GemmArgs p1 = g1, p2 = g2;
+  p1.tiles = p2.tiles = q.ptiles;
+  p1.num_tiles = p2.num_tiles = q.num_ptiles;
   if (e == cudaSuccess) {
-    if (paired) {
-      GemmArgs gp = g1;
-      gp.tiles = q.ptiles;
-      gp.num_tiles = q.num_ptiles;
-      e = launch_gemm1_swiglu_paired(tm_x, *a.tm_w13, gp, o);
-    } else {
+    if (pairs && sp.s1 == 1)
+      e = launch_gemm1_swiglu_pair(tm_x, *a.tm_w13, p1, o);
+    else
       e = launch_gemm1_swiglu(tm_x, *a.tm_w13, g1, o);
-    }
   }
   mark(RIMURU_K_GEMM1, 1);
   mark(RIMURU_K_GEMM2, 0);
-  if (e == cudaSuccess) e = launch_gemm2(tm_h, *a.tm_w2, g2, o);
+  if (e == cudaSuccess) {
+    if (pairs && sp.s2 == 1)
+      e = launch_gemm2_pair(tm_h, *a.tm_w2, p2, o);
+    else
+      e = launch_gemm2(tm_h, *a.tm_w2, g2, o);
+  }
   mark(RIMURU_K_GEMM2, 1);
   mark(RIMURU_K_COMBINE, 0);
   if (e == cudaSuccess)
