@@ -124,7 +124,9 @@ def source_digest(*rel_paths):
     return h.hexdigest()[:16]
 
 
-GEMM_SOURCES = ("paged_moe_shared_gb300/csrc/moe_gemm.cu", "paged_moe_shared_gb300/csrc/device.cuh")
+GEMM_SOURCES = ("paged_moe_shared_gb300/csrc/moe_gemm.cu",
+                "paged_moe_shared_gb300/csrc/moe_gemm_2sm.cu",
+                "paged_moe_shared_gb300/csrc/device.cuh")
 
 
 def ncu_traffic(kernel: str, workload: str):
