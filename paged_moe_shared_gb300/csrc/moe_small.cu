@@ -71,8 +71,9 @@ __device__ __forceinline__ void route_token(const float* __restrict__ row, int E
     }
   }
   if (__any_sync(kFull, bad) && lane == 0) set_error(err, RIMURU_DEV_NONFINITE);
-  uint32_t taken = 0;
-  float mx = 0.f, psum = 0.f, my_p = 0.f;
+  // k selection rounds; lane j keeps the logit and expert of slot j, and the
+  // exponentials are taken afterwards, one per lane, instead of once per round.
+  uint32_t taken = 0, my_key = 0u;
   my_id = 0;
   for (int j = 0; j < k; ++j) {
     uint32_t bk = 0u, bi = 0xffffffffu;
@@ -85,16 +86,19 @@ __device__ __forceinline__ void route_token(const float* __restrict__ row, int E
     }
     const uint32_t m = __reduce_max_sync(kFull, bk);
     const uint32_t win = __reduce_min_sync(kFull, bk == m ? bi : 0xffffffffu);
-    const float v = key_value(m);
-    if (j == 0) mx = (v == -INFINITY) ? 0.f : v;  // largest logit of the token
     if (static_cast<int>(win & 31u) == lane) taken |= 1u << (win >> 5);
-    const float p = expf(v - mx);
-    psum += p;
     if (lane == j) {
       my_id = static_cast<int>(win);
-      my_p = p;
+      my_key = m;
     }
   }
+  // largest logit of the token: slot 0's (0 if it is -inf, i.e. no finite logit)
+  const float top = key_value(__shfl_sync(kFull, my_key, 0));
+  const float mx = (top == -INFINITY) ? 0.f : top;
+  const float my_p = lane < k ? expf(key_value(my_key) - mx) : 0.f;
+  float psum = my_p;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) psum += __shfl_xor_sync(kFull, psum, off);
   float denom = psum;
   if (!renorm) {
     float s = 0.f;
