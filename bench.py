@@ -2,8 +2,9 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-A step is one pass of the whole layer (route, align, gather, GEMM 1 + SwiGLU, GEMM 2,
-combine) over one batch of synthetic tokens, through the C ABI on device-resident inputs.
+A step is one pass of the whole layer (route, align, GEMM 1 + SwiGLU with the gather of its
+rows, GEMM 2, combine) over one batch of synthetic tokens, through the C ABI on device-resident
+inputs.
 The default workload is the Qwen3-30B-A3B-shaped layer with 64 decode tokens; its expert
 pages (about 1.2 GB touched per step) exceed the 129 MB L2, so no flush is needed between
 steps.  Rank 0 prints one JSON line.  ``--impl reference`` times the CPU oracle on the
@@ -29,8 +30,7 @@ METRIC = "paged fused-MoE tokens/s; % of HBM / bf16 tensor roofline (Qwen3-30B-A
 DEFAULT_STEPS = {"q3_decode": 2000, "q3_prefill_zipf": 100, "q35_mixed_pool": 500, "tiny": 2000,
                  "q3_stack_offload": 32}
 # kernels one layer launches, in order
-LAYER_KERNELS = ("moe_route", "moe_align", "moe_gather", "moe_gemm1_swiglu", "moe_gemm2",
-                 "moe_combine")
+LAYER_KERNELS = ("moe_route", "moe_align", "moe_gemm1_swiglu", "moe_gemm2", "moe_combine")
 PROFILE_EVERY = 10      # timed forwards per forward whose dominant kernel is bracketed
 REF_DEFAULT_STEPS = 20  # oracle steps when --impl reference is given no --steps
 REF_SECONDS = 120.0     # host time the oracle arm aims for, warm-up included

@@ -109,6 +109,27 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// ------------------------------------------------------------- cp.async
+// 16-byte global -> shared copy through the L1-bypassing path (generic proxy).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// One arrival on `bar` once every cp.async this thread issued so far has
+// landed; the barrier's expected count includes these arrivals (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+// Makes shared-memory writes of the generic proxy (st.shared, cp.async) that
+// this thread has observed visible to its later async-proxy operations
+// (tcgen05.mma operand reads, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------- tcgen05
 // TMEM allocation is done by one full warp; the address lands in shared memory.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {

@@ -93,6 +93,11 @@ struct GemmArgs {
   int part_rows;              // rows of one partial slab (>= rows of any tile)
   float* part;                // [tiles * splits][part_rows][256] fp32 partials
   int32_t* tile_cnt;          // [tiles] finished splits per tile (zeroed by align)
+  // GEMM 1 with gathered A: row r of the sorted order is row sorted[r] / top_k of x
+  const __nv_bfloat16* x;     // [T][ldx]
+  const int32_t* sorted;      // [A]
+  int top_k;
+  int ldx;
 };
 
 // a3: h = silu(x_sorted w1_e) * (x_sorted w3_e); w1/w3 read in place from pages.
@@ -101,6 +106,11 @@ cudaError_t launch_gemm1_swiglu(const CUtensorMap& tm_x, const CUtensorMap& tm_w
 // Use the CTA-pair GEMMs when the assignments average at least this many
 // 128-row blocks per expert (most experts then have pairs of blocks).
 constexpr int kPairMinBlocksPerExpert = 2;
+
+// a3 with the gather fused in: four loader warps copy each A stage straight
+// from x (cp.async) using `sorted`, so x_sorted is neither written nor read.
+cudaError_t launch_gemm1_swiglu_gather(const CUtensorMap& tm_w13, const GemmArgs& a,
+                                       const LaunchOpts& o);
 
 // a3 and a4 for large batches on CTA pairs (tcgen05 cta_group::2): a tile is
 // one entry of the pair table (tiles/num_tiles in `a` name it) times one

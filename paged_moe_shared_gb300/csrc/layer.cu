@@ -181,6 +181,10 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   GemmArgs g2 = g1;
   g1.splits = sp.s1;
   g1.tile_cnt = q.tile_cnt;
+  g1.x = static_cast<const __nv_bfloat16*>(a.x);
+  g1.sorted = q.sorted;
+  g1.top_k = k;
+  g1.ldx = H;
   g2.splits = sp.s2;
   g2.tile_cnt = q.tile_cnt + std::max(sp.t1, sp.t2);
   g1.out = q.h;
@@ -205,12 +209,9 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
       if (which == 1 && a.hits) *a.hits |= 1u << kidx;
     }
   };
-  if (!gathered) {
-    mark(RIMURU_K_GATHER, 0);
-    if (e == cudaSuccess)
-      e = launch_gather(static_cast<const __nv_bfloat16*>(a.x), q.sorted, A, k, H, q.xs, gather_o);
-    mark(RIMURU_K_GATHER, 1);
-  }
+  // Batches past the small-batch kernel gather A inside GEMM 1; the small-batch
+  // kernel has already written x_sorted.
+  const bool gather_in_gemm = !gathered;
   mark(RIMURU_K_GEMM1, 0);
   // Large batches (at least two 128-row blocks per expert on average) run both
   // GEMMs on CTA pairs over the table of 256-row pairs of blocks.
@@ -220,10 +221,14 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   p1.tiles = p2.tiles = q.ptiles;
   p1.num_tiles = p2.num_tiles = q.num_ptiles;
   if (e == cudaSuccess) {
-    if (pairs && sp.s1 == 1)
-      e = launch_gemm1_swiglu_pair(tm_x, *a.tm_w13, p1, o);
+    LaunchOpts o1 = o;
+    o1.pdl = gather_o.pdl;  // GEMM 1 follows align directly, or host-side work
+    if (gather_in_gemm)
+      e = launch_gemm1_swiglu_gather(*a.tm_w13, g1, o1);
+    else if (pairs && sp.s1 == 1)
+      e = launch_gemm1_swiglu_pair(tm_x, *a.tm_w13, p1, o1);
     else
-      e = launch_gemm1_swiglu(tm_x, *a.tm_w13, g1, o);
+      e = launch_gemm1_swiglu(tm_x, *a.tm_w13, g1, o1);
   }
   mark(RIMURU_K_GEMM1, 1);
   mark(RIMURU_K_GEMM2, 0);

@@ -40,6 +40,9 @@ constexpr int kBChunk = BK * 64 * 2;         // 8 KiB: [64 k rows][64 cols] of o
 constexpr int kBBytes = 4 * kBChunk;         // 32 KiB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
+// GEMM 1 with its A rows gathered from x by four more warps (cp.async): 320.
+constexpr int kLoaderWarps = 4;
+constexpr int kThreadsGather = kThreads + 32 * kLoaderWarps;
 constexpr int kTmemCols = 2 * BN;            // two accumulators
 // Epilogue staging: per epilogue warp one 32-row x 64-column bf16 block (4 KiB),
 // 128-byte rows with 16-byte chunks XOR-swizzled by row so that both the
@@ -59,8 +62,8 @@ struct Shared {
   int last;  // split-K: this CTA finished the last split of the current tile
 };
 
-template <bool kSwiGLU>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kSwiGLU, bool kGatherA>
+__global__ void __launch_bounds__(kGatherA ? kThreadsGather : kThreads, 1)
     paged_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
                       const __grid_constant__ CUtensorMap tm_w, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -75,7 +78,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sh->full[s], 1);
+      // the producer's armed arrival, plus one per loader thread when A is gathered
+      mbar_init(&sh->full[s], kGatherA ? 1 + 32 * kLoaderWarps : 1);
       mbar_init(&sh->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -85,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     fence_barrier_init();
-    prefetch_tmap(&tm_act);
+    if (!kGatherA) prefetch_tmap(&tm_act);
     prefetch_tmap(&tm_w);
   }
   if (warp == 1) {
@@ -134,8 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
-          tma_load_2d(sA + s * kABytes, &tm_act, &sh->full[s], kb * BK, row0, pol_a);
+          mbar_arrive_expect_tx(&sh->full[s], kGatherA ? kBBytes : kStageBytes);
+          if (!kGatherA) tma_load_2d(sA + s * kABytes, &tm_act, &sh->full[s], kb * BK, row0, pol_a);
           uint8_t* b = sB + s * kBBytes;
           if (kSwiGLU) {
             tma_load_3d(b + 0 * kBChunk, &tm_w, &sh->full[s], n0, kb * BK, pg0, pol_w);
@@ -182,6 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          // A arrived through cp.async (generic proxy); the MMA reads it
+          // through the async proxy
+          if (kGatherA) fence_proxy_async_smem();
           const uint32_t a0 = smem_u32(sA + s * kABytes);
           const uint32_t b0 = smem_u32(sB + s * kBBytes);
 #pragma unroll
@@ -207,6 +214,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int never = 0;
       mbar_wait(&sh->drain, 0, &never);
     }
+  } else if (kGatherA && warp >= 6) {
+    // ----------------------------------------------------------- A loaders
+    // Warp 6 + w copies rows 32 w .. 32 w + 31 of each A stage straight from x:
+    // row r of the tile is token sorted[row0 + r] / top_k.  Eight lanes cover
+    // one row's 128 bytes, written at the 128-byte-swizzled position the MMA
+    // descriptor expects (16-byte chunk c of row r at chunk c ^ (r % 8)).
+    // Rows past the tile's expert repeat its last row (their results are not
+    // stored).  Each thread's arrival on the stage's full barrier fires when
+    // its copies have landed.
+    const int lw = warp - 6, sub = lane >> 3, chunk = lane & 7;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+      const int tile = u / S, split = u - tile * S;
+      const int kb0 = split * nkb / S, kb1 = (split + 1) * nkb / S;
+      const int mb = tile / p.n_blocks;
+      const int e = p.tiles[2 * mb], row0 = p.tiles[2 * mb + 1];
+      const int rows = min(BM, p.offsets[e + 1] - row0);  // >= 1 for a listed tile
+      const __nv_bfloat16* src[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = min(32 * lw + 4 * i + sub, rows - 1);
+        src[i] = p.x + static_cast<size_t>(p.sorted[row0 + r] / p.top_k) * p.ldx + chunk * 8;
+      }
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+        bool got = true;
+        if (lane == 0) got = mbar_wait(&sh->empty[s], ph ^ 1u, abort);
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t a_s = smem_u32(sA + s * kABytes);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 32 * lw + 4 * i + sub;
+          cp_async16(a_s + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * BK);
+        }
+        cp_async_arrive_noinc(&sh->full[s]);
+      }
+    }
+    if (!ok && lane == 0) {
+      set_error(p.err, RIMURU_DEV_TIMEOUT);
+      sh->abort = 1;
+    }
+    cp_async_wait_all();  // no copy of this thread is in flight when the CTA exits
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may read
@@ -363,12 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kSwiGLU>
+template <bool kSwiGLU, bool kGatherA>
 cudaError_t launch_gemm(const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a,
                         const LaunchOpts& o) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t st = cudaFuncSetAttribute(paged_gemm_kernel<kSwiGLU>,
+    cudaError_t st = cudaFuncSetAttribute(paged_gemm_kernel<kSwiGLU, kGatherA>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (st != cudaSuccess) return st;
     configured = true;
@@ -377,7 +430,7 @@ cudaError_t launch_gemm(const CUtensorMap& tm_act, const CUtensorMap& tm_w, cons
   const int grid = static_cast<int>(tiles < o.sm_count ? tiles : o.sm_count);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid > 0 ? grid : 1);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kGatherA ? kThreadsGather : kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = o.stream;
   cudaLaunchAttribute attr[1];
@@ -385,19 +438,24 @@ cudaError_t launch_gemm(const CUtensorMap& tm_act, const CUtensorMap& tm_w, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = o.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, paged_gemm_kernel<kSwiGLU>, tm_act, tm_w, a);
+  return cudaLaunchKernelEx(&cfg, paged_gemm_kernel<kSwiGLU, kGatherA>, tm_act, tm_w, a);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm1_swiglu(const CUtensorMap& tm_x, const CUtensorMap& tm_w13,
                                 const GemmArgs& a, const LaunchOpts& o) {
-  return launch_gemm<true>(tm_x, tm_w13, a, o);
+  return launch_gemm<true, false>(tm_x, tm_w13, a, o);
+}
+
+cudaError_t launch_gemm1_swiglu_gather(const CUtensorMap& tm_w13, const GemmArgs& a,
+                                       const LaunchOpts& o) {
+  return launch_gemm<true, true>(tm_w13, tm_w13, a, o);  // the activation map is not used
 }
 
 cudaError_t launch_gemm2(const CUtensorMap& tm_h, const CUtensorMap& tm_w2, const GemmArgs& a,
                          const LaunchOpts& o) {
-  return launch_gemm<false>(tm_h, tm_w2, a, o);
+  return launch_gemm<false, false>(tm_h, tm_w2, a, o);
 }
 
 }  // namespace rimuru
