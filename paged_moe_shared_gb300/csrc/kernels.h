@@ -72,9 +72,6 @@ cudaError_t launch_route_align_gather(const float* logits, const __nv_bfloat16* 
                                       int32_t* num_ptiles, int32_t* tile_cnt, int cnt_len,
                                       __nv_bfloat16* x_sorted, int* err, const LaunchOpts& o);
 
-// x rows in expert-sorted order: x_sorted[r] = x[sorted[r] / k].
-cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted, int A, int k, int H,
-                          __nv_bfloat16* x_sorted, const LaunchOpts& o);
 
 struct GemmArgs {
   const int32_t* page_table;  // [E][3] of the layer
@@ -103,7 +100,7 @@ struct GemmArgs {
 // a3: h = silu(x_sorted w1_e) * (x_sorted w3_e); w1/w3 read in place from pages.
 cudaError_t launch_gemm1_swiglu(const CUtensorMap& tm_x, const CUtensorMap& tm_w13,
                                 const GemmArgs& a, const LaunchOpts& o);
-// Use the CTA-pair GEMMs when the assignments average at least this many
+// Use the CTA-pair GEMM 2 when the assignments average at least this many
 // 128-row blocks per expert (most experts then have pairs of blocks).
 constexpr int kPairMinBlocksPerExpert = 2;
 
@@ -112,11 +109,9 @@ constexpr int kPairMinBlocksPerExpert = 2;
 cudaError_t launch_gemm1_swiglu_gather(const CUtensorMap& tm_w13, const GemmArgs& a,
                                        const LaunchOpts& o);
 
-// a3 and a4 for large batches on CTA pairs (tcgen05 cta_group::2): a tile is
-// one entry of the pair table (tiles/num_tiles in `a` name it) times one
-// column block; each CTA stages half of every weight tile.
-cudaError_t launch_gemm1_swiglu_pair(const CUtensorMap& tm_x, const CUtensorMap& tm_w13,
-                                     const GemmArgs& a, const LaunchOpts& o);
+// a4 for large batches on CTA pairs (tcgen05 cta_group::2): a tile is one
+// entry of the pair table (tiles/num_tiles in `a` name it) times one column
+// block; each CTA stages half of every weight tile.
 cudaError_t launch_gemm2_pair(const CUtensorMap& tm_h, const CUtensorMap& tm_w2, const GemmArgs& a,
                               const LaunchOpts& o);
 
@@ -159,9 +154,9 @@ struct LayerLaunch {
 
 // Launch the six kernels of one layer.  Returns a rimuru status.
 int launch_layer(const LayerLaunch& a);
-// The same in two halves: routing (route, align) and the expert part (gather,
-// GEMM 1, GEMM 2, combine).  Host-side work may sit between the two;
-// after_route = false when it does (the gather then follows it in stream order).
+// The same in two halves: routing (route, align) and the expert part (GEMM 1,
+// GEMM 2, combine).  Host-side work may sit between the two; after_route =
+// false when it does (GEMM 1 then follows it in plain stream order).
 int launch_layer_route(const LayerLaunch& a);
 // gathered = true when x_sorted is already written (the small-batch kernel).
 int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered = false);

@@ -200,8 +200,6 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   o.stream = a.stream;
   o.sm_count = a.sm_count;
   o.pdl = a.pdl;
-  LaunchOpts gather_o = o;
-  gather_o.pdl = after_route && a.pdl;  // directly behind align, or behind host-side work
   cudaError_t e = cudaSuccess;
   auto mark = [&](int kidx, int which) {
     if (a.ev && (a.ev_mask >> kidx & 1u) && e == cudaSuccess) {
@@ -209,26 +207,23 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
       if (which == 1 && a.hits) *a.hits |= 1u << kidx;
     }
   };
-  // Batches past the small-batch kernel gather A inside GEMM 1; the small-batch
-  // kernel has already written x_sorted.
-  const bool gather_in_gemm = !gathered;
   mark(RIMURU_K_GEMM1, 0);
-  // Large batches (at least two 128-row blocks per expert on average) run both
-  // GEMMs on CTA pairs over the table of 256-row pairs of blocks.
+  // Large batches (at least two 128-row blocks per expert on average) run
+  // GEMM 2 on CTA pairs over the table of 256-row pairs of blocks.
   const bool pairs = static_cast<long long>(A) >=
                      static_cast<long long>(kPairMinBlocksPerExpert) * kTileM * E;
-  GemmArgs p1 = g1, p2 = g2;
-  p1.tiles = p2.tiles = q.ptiles;
-  p1.num_tiles = p2.num_tiles = q.num_ptiles;
+  GemmArgs p2 = g2;
+  p2.tiles = q.ptiles;
+  p2.num_tiles = q.num_ptiles;
+  // GEMM 1 gathers its rows from x, except behind the small-batch kernel,
+  // which has written x_sorted already.
   if (e == cudaSuccess) {
     LaunchOpts o1 = o;
-    o1.pdl = gather_o.pdl;  // GEMM 1 follows align directly, or host-side work
-    if (gather_in_gemm)
-      e = launch_gemm1_swiglu_gather(*a.tm_w13, g1, o1);
-    else if (pairs && sp.s1 == 1)
-      e = launch_gemm1_swiglu_pair(tm_x, *a.tm_w13, p1, o1);
-    else
+    o1.pdl = after_route && a.pdl;  // behind align or the small-batch kernel; not behind host work
+    if (gathered)
       e = launch_gemm1_swiglu(tm_x, *a.tm_w13, g1, o1);
+    else
+      e = launch_gemm1_swiglu_gather(*a.tm_w13, g1, o1);
   }
   mark(RIMURU_K_GEMM1, 1);
   mark(RIMURU_K_GEMM2, 0);

@@ -1,29 +1,25 @@
-// Paged grouped GEMMs for large batches on CTA pairs (tcgen05 cta_group::2).
+// GEMM 2 of the paged fused MoE layer for large batches, on CTA pairs
+// (tcgen05 cta_group::2).
 //
-// The computation is that of paged_gemm_kernel (moe_gemm.cu): GEMM 1 writes
-// h = silu(x w1_e) * (x w3_e), GEMM 2 writes y = h w2_e, with the expert's
-// weights read in place from their pool pages through the 3-D tensor map over
+// The computation is that of paged_gemm_kernel<false> (moe_gemm.cu): y = h w2_e
+// with w2_e read in place from its pool page through the 3-D tensor map over
 // the pool (page coordinate = page-table entry; Rimuru, abstract and the
 // explainer page's paragraph on the fused MoE kernel).
 //
 // What changes is the operand traffic per SM.  A cluster of two CTAs on two
 // SMs computes one 256-row x 256-column tile with M = 256 MMAs: each CTA
-// stages its own 128 rows of A and only half (128 columns) of the weight
-// tile, and the pair's MMAs read the other half from the peer.  A 64-deep k
-// block costs each SM 32 KiB of loads instead of 48 KiB for the same MMA work,
-// which matters because large batches are limited by operand delivery into
-// shared memory, not by the tensor pipe; the smaller stages also let six of
-// them be in flight.  Each CTA's TMEM holds the 128 x 256 fp32 accumulator of
-// its own rows, double-buffered, so the epilogue still overlaps the next
-// tile's main loop.
+// stages its own 128 rows of h and only 128 of the tile's 256 weight columns,
+// and the pair's MMAs read the other half from the peer.  A 64-deep k block
+// costs each SM 32 KiB of loads instead of 48 KiB for the same MMA work, which
+// matters because large batches are limited by shared-memory traffic, not by
+// the tensor pipe; the smaller stages also let six of them be in flight.  Each
+// CTA's TMEM holds the 128 x 256 fp32 accumulator of its own rows,
+// double-buffered, so the epilogue still overlaps the next tile's main loop.
 //
 // A tile is one entry of the pair table written by moe_align (two 128-row
 // blocks of the same expert; an expert's odd last block is paired with the
 // rows that follow it, which are computed and not stored) times one column
-// block.  GEMM 1: the rank-0 CTA stages 128 columns of w1, the rank-1 CTA the
-// same columns of w3, so accumulator columns 0..127 are the gate and 128..255
-// the up projection in both CTAs.  GEMM 2: rank r stages columns
-// 128 r .. 128 r + 127 of the 256-column block of w2.
+// block.  Rank r stages columns 128 r .. 128 r + 127 of the 256-column block.
 //
 // Synchronisation: the full barrier of a stage lives in the rank-0 CTA and
 // counts both CTAs' bytes (each producer arms it for its own loads); the MMA
@@ -75,9 +71,8 @@ __device__ __forceinline__ void abort_pair(Shared* sh, int* err) {
   st_cluster_u32(cluster_addr(&sh->abort, cluster_rank() ^ 1u), 1u);
 }
 
-template <bool kSwiGLU>
 __global__ void __launch_bounds__(kThreads, 1)
-    pair_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
+    pair_gemm2_kernel(const __grid_constant__ CUtensorMap tm_act,
                      const __grid_constant__ CUtensorMap tm_w, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -131,14 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pt = u / p.n_blocks, nb = u % p.n_blocks;
         const int e = p.tiles[2 * pt];
         const int row0 = p.tiles[2 * pt + 1] + static_cast<int>(rank) * BM;
-        int pg, n0;
-        if (kSwiGLU) {
-          pg = p.page_table[3 * e + (rank == 0 ? RIMURU_PROJ_W1 : RIMURU_PROJ_W3)];
-          n0 = nb * (BN / 2);
-        } else {
-          pg = p.page_table[3 * e + RIMURU_PROJ_W2];
-          n0 = nb * BN + static_cast<int>(rank) * (BN / 2);
-        }
+        int pg = p.page_table[3 * e + RIMURU_PROJ_W2];
+        const int n0 = nb * BN + static_cast<int>(rank) * (BN / 2);
         if (pg < 0 || pg >= p.num_pages) {
           set_error(p.err, RIMURU_DEV_BAD_PAGE);  // host checks make this unreachable
           pg = 0;
@@ -226,34 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row0 = p.tiles[2 * pt + 1] + static_cast<int>(rank) * BM;
       const int rows = min(BM, p.offsets[e + 1] - row0);  // <= 0: rows of the next expert
       const uint32_t tb = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-      if (kSwiGLU) {
-        // GEMM 1: each lane writes its own row of h, 32 columns at a time.
-        const int r = q * 32 + lane;
-        __nv_bfloat16* orow = p.out + static_cast<size_t>(row0 + r) * p.ldo;
-        const int n0 = nb * (BN / 2);
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
-          uint32_t g[32], v[32];
-          tmem_ld32(tb + c0, g);
-          tmem_ld32(tb + BN / 2 + c0, v);
-          tmem_ld_wait();
-          if (r < rows) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t o[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int c = 8 * j + 2 * i;
-                o[i] = pack_bf16x2(silu_mul(__uint_as_float(g[c]), __uint_as_float(v[c])),
-                                   silu_mul(__uint_as_float(g[c + 1]), __uint_as_float(v[c + 1])));
-              }
-              dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-          }
-        }
-      } else {
-        // GEMM 2: rows q*32 .. q*32+31 go out in blocks of 64 columns through a
+      {
+        // Rows q*32 .. q*32+31 go out in blocks of 64 columns through a
         // row-swizzled staging block, four full 128-byte row segments per store.
         const uint32_t blk_s = smem_u32(sOut + (warp - 2) * kStageOutBytes);
         const int n0 = nb * BN;
@@ -311,7 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kSwiGLU>
 int max_pair_clusters(const LaunchOpts& o) {
   static int cached = -1;
   if (cached < 0) {
@@ -327,25 +289,24 @@ int max_pair_clusters(const LaunchOpts& o) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<kSwiGLU>, &cfg) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm2_kernel, &cfg) != cudaSuccess || n < 1)
       n = o.sm_count / 2;
     cached = n;
   }
   return cached;
 }
 
-template <bool kSwiGLU>
 cudaError_t launch_pair(const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a,
                         const LaunchOpts& o) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t st = cudaFuncSetAttribute(pair_gemm_kernel<kSwiGLU>,
+    cudaError_t st = cudaFuncSetAttribute(pair_gemm2_kernel,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (st != cudaSuccess) return st;
     configured = true;
   }
   const long long tiles = static_cast<long long>(a.max_tiles) * a.n_blocks;
-  const int clusters_cap = max_pair_clusters<kSwiGLU>(o);
+  const int clusters_cap = max_pair_clusters(o);
   const int clusters = static_cast<int>(tiles < clusters_cap ? tiles : clusters_cap);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (clusters > 0 ? clusters : 1));
@@ -361,19 +322,14 @@ cudaError_t launch_pair(const CUtensorMap& tm_act, const CUtensorMap& tm_w, cons
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = o.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<kSwiGLU>, tm_act, tm_w, a);
+  return cudaLaunchKernelEx(&cfg, pair_gemm2_kernel, tm_act, tm_w, a);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm1_swiglu_pair(const CUtensorMap& tm_x, const CUtensorMap& tm_w13,
-                                     const GemmArgs& a, const LaunchOpts& o) {
-  return launch_pair<true>(tm_x, tm_w13, a, o);
-}
-
 cudaError_t launch_gemm2_pair(const CUtensorMap& tm_h, const CUtensorMap& tm_w2, const GemmArgs& a,
                               const LaunchOpts& o) {
-  return launch_pair<false>(tm_h, tm_w2, a, o);
+  return launch_pair(tm_h, tm_w2, a, o);
 }
 
 }  // namespace rimuru

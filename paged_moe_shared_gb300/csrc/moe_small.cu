@@ -266,35 +266,6 @@ __global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
   }
 }
 
-// ----------------------------------------------------------------- gather
-// Each CTA copies kGatherRows rows per iteration, with every load issued
-// before the first store so several 16-byte loads per thread are in flight.
-// x_sorted is written once and read once by GEMM 1, so the stores are
-// streaming (evict-first): at 8192 tokens this takes the gather of 268 MB from
-// 64 to 52 us.
-constexpr int kGatherRows = 8;
-
-__global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict__ x,
-                                                         const int32_t* __restrict__ sorted, int A,
-                                                         int k, int H8, uint4* __restrict__ xs) {
-  grid_dep_wait();
-  grid_dep_launch();
-  for (int r0 = blockIdx.x * kGatherRows; r0 < A; r0 += gridDim.x * kGatherRows) {
-    int t[kGatherRows];
-#pragma unroll
-    for (int i = 0; i < kGatherRows; ++i) t[i] = (r0 + i < A) ? sorted[r0 + i] / k : -1;
-    for (int c = threadIdx.x; c < H8; c += blockDim.x) {
-      uint4 v[kGatherRows];
-#pragma unroll
-      for (int i = 0; i < kGatherRows; ++i)
-        if (t[i] >= 0) v[i] = x[static_cast<size_t>(t[i]) * H8 + c];
-#pragma unroll
-      for (int i = 0; i < kGatherRows; ++i)
-        if (t[i] >= 0) __stcs(&xs[static_cast<size_t>(r0 + i) * H8 + c], v[i]);
-    }
-  }
-}
-
 // ----------------------------------------------------- small batches, one launch
 // Route, align and gather in one kernel when all A = T * k assignments fit one
 // CTA (A <= kChunkAssign, decode-sized batches).  Every CTA routes all T tokens
@@ -474,14 +445,6 @@ cudaError_t launch_align(const int32_t* ids, const int32_t* chunk_hist, int chun
   return launch(moe_align_kernel, dim3(chunks), dim3(kChunkAssign), 0, o, ids, chunk_hist, chunks,
                 A, E, chunk, offsets, sorted, inv, tiles, num_tiles, ptiles, num_ptiles, tile_cnt,
                 cnt_len, err);
-}
-
-cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* sorted, int A, int k, int H,
-                          __nv_bfloat16* x_sorted, const LaunchOpts& o) {
-  const int blocks = (A + kGatherRows - 1) / kGatherRows;
-  const int grid = min(blocks, o.sm_count * 8);
-  return launch(moe_gather_kernel, dim3(grid), dim3(256), 0, o, reinterpret_cast<const uint4*>(x),
-                sorted, A, k, H / 8, reinterpret_cast<uint4*>(x_sorted));
 }
 
 cudaError_t launch_route_align_gather(const float* logits, const __nv_bfloat16* x, int T, int E,
