@@ -451,11 +451,13 @@ int rimuru_get_device_error(rimuru_view_t view, int* code, int clear);
 
 /* ------------------------------------------------------------- profiling */
 
-/* Kernel slots of one forward.  A forward launches route, align, gather,
- * GEMM 1, GEMM 2, combine in that order, except when its T * top_k
- * assignments fit one CTA (at most 1024): then one kernel in slot
- * RIMURU_K_ROUTE_ALIGN_GATHER does the first three steps, followed by GEMM 1,
- * GEMM 2 and combine. */
+/* Kernel slots of one forward.  When its T * top_k assignments fit one CTA
+ * (at most 1024), a forward launches the kernel in slot
+ * RIMURU_K_ROUTE_ALIGN_GATHER (routing, grouping and the gather of x rows),
+ * then GEMM 1, GEMM 2 and combine; otherwise route, align, GEMM 1 (which
+ * gathers its rows from x itself), GEMM 2 and combine.  No current launch
+ * sequence uses slot RIMURU_K_GATHER (a separate gather kernel); the slot
+ * keeps the numbering of the others and always reports 0 launches. */
 enum {
   RIMURU_K_ROUTE = 0,
   RIMURU_K_ALIGN = 1,
