@@ -246,9 +246,17 @@ def _wide_inter_t1():
     return wl.build_simple("wide_inter", shape, 1, pool_pages=16, seed=9)
 
 
+def _gathered_split():
+    # 1200 assignments (past the small-batch kernel, so GEMM 1 gathers its rows) over 8
+    # experts with H = 1024: few enough tiles for GEMM 1 to split its 16 k blocks in two
+    shape = wl.MoEShape(H=1024, I=128, E=8, k=2)
+    return wl.build_simple("gathered_split", shape, 600, pool_pages=32, seed=10)
+
+
 @pytest.mark.parametrize("make", [lambda: wl.q35_mixed_pool(0, T=1), lambda: wl.q3_decode(0, T=1),
-                                  _wide_inter_t1],
-                         ids=["q35_T1_gemm1_split", "q3_T1_gemm1_split", "wide_inter_gemm2_split"])
+                                  _wide_inter_t1, _gathered_split],
+                         ids=["q35_T1_gemm1_split", "q3_T1_gemm1_split", "wide_inter_gemm2_split",
+                              "gathered_gemm1_split"])
 def test_split_k_is_used_for_few_tiles_and_is_deterministic(oracle, make):
     """With few tiles the GEMMs split K over several CTAs and sum the fp32 partials in split
     order, so repeated forwards agree bit for bit."""
