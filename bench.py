@@ -164,7 +164,6 @@ def kernel_work(w, counts):
     return {
         "moe_route": {"bytes": T * E * 4 + A * 8, "flops": 0},
         "moe_align": {"bytes": A * 4 * 3, "flops": 0},
-        "moe_gather": {"bytes": 2 * A * H * 2, "flops": 0},
         "moe_route_align_gather": {"bytes": T * E * 4 + A * 8 + A * 4 * 3 + 2 * A * H * 2,
                                    "flops": 0},
         "moe_gemm1_swiglu": {"bytes": U * 2 * H * I * 2 + A * H * 2 + A * I * 2,

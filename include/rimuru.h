@@ -245,7 +245,8 @@ typedef struct rimuru_ws_layout {
   uint64_t inv;        /* int32 [A]: sorted row of assignment f */
   uint64_t tiles;      /* int32 [max_tiles][2]: (expert, first sorted row) of each 128-row block */
   uint64_t num_tiles;  /* int32: number of valid row blocks */
-  uint64_t x_sorted;   /* bf16 [A][hidden]: x rows in sorted order */
+  uint64_t x_sorted;   /* bf16 [A][hidden]: x rows in sorted order, only when A <= 1024
+                          (empty region otherwise: GEMM 1 then gathers rows from x) */
   uint64_t h;          /* bf16 [A][inter]: silu(x w1) * (x w3) in sorted order */
   uint64_t y;          /* bf16 [A][hidden]: h w2 in sorted order (unweighted) */
   uint64_t ptiles;     /* int32 [max_tiles][2]: (expert, first row) of each 256-row pair of blocks */
@@ -337,7 +338,7 @@ int rimuru_moe_forward_host(const void* x_host, const float* logits_host, int nu
  * makes no cudaMalloc, cudaFree, cudaMallocHost or other allocating call.
  * A forward whose workspace (rimuru_moe_workspace_bytes) plus 8.25 KiB does
  * not fit is rejected with RIMURU_ERR_WORKSPACE before anything is launched
- * (about 200 tokens at hidden 2048 / inter 768 / top-8).
+ * (about 370 tokens at hidden 2048 / inter 768 / top-8).
  * First call on a device: it looks up the array's device address
  * (cudaGetSymbolAddress) with that device current and caches it; make that
  * first call before any stream capture.

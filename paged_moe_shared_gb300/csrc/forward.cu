@@ -73,7 +73,9 @@ void layout_for(const View& v, int T, rimuru_ws_layout* L) {
   L->inv = take(A * 4);
   L->tiles = take(max_tiles * 2 * 4);
   L->num_tiles = take(16);
-  L->x_sorted = take(A * v.hidden * 2);
+  // x rows in sorted order exist only for batches the small-batch kernel
+  // handles; past that, GEMM 1 gathers its rows from x itself
+  L->x_sorted = take(A <= static_cast<uint64_t>(kChunkAssign) ? A * v.hidden * 2 : 0);
   L->h = take(A * v.inter * 2);
   L->y = take(A * v.hidden * 2);
   // split-K bookkeeping (see split_count): counters for both GEMMs, one slab

@@ -1,6 +1,7 @@
 """Runs one forward of the paged fused-MoE layer through the C ABI and returns every
 intermediate the workspace holds (routing ids and weights, offsets, the permutation and
-its inverse, the tile table, x_sorted, h, y) plus the output, all as numpy arrays."""
+its inverse, the tile table, h, y; x_sorted for batches of at most 1024 assignments) plus the
+output, all as numpy arrays."""
 from __future__ import annotations
 
 import numpy as np
@@ -60,7 +61,8 @@ class Runner:
             "num_tiles": int(self.region("num_tiles", torch.int32, 1).cpu().item()),
             "h": to_f64(self.region("h", torch.bfloat16, A * s.I).view(A, s.I)),
             "y": to_f64(self.region("y", torch.bfloat16, A * s.H).view(A, s.H)),
-            "x_sorted": self.region("x_sorted", torch.bfloat16, A * s.H).view(A, s.H),
+            "x_sorted": (self.region("x_sorted", torch.bfloat16, A * s.H).view(A, s.H)
+                         if A <= 1024 else None),
             "dev_err": R.rimuru_get_device_error(self.ev, clear=True),
         }
         r["tiles"] = self.region("tiles", torch.int32, 2 * r["num_tiles"]).cpu().numpy().reshape(-1, 2)

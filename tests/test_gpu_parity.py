@@ -275,10 +275,11 @@ def test_split_k_is_used_for_few_tiles_and_is_deterministic(oracle, make):
         assert np.array_equal(a[key], b[key]), key
 
 
-def test_paired_gemm1_with_odd_and_even_block_counts(oracle):
+def test_cta_pair_gemm2_with_odd_and_even_block_counts(oracle):
     """1500 tokens of the tiny layer (3000 assignments, at least two 128-row blocks per
-    expert on average) take the GEMM 1 variant that pairs two row blocks of an expert per
-    CTA; a bias makes one expert hot (many blocks) and others small (a lone last block)."""
+    expert on average) run GEMM 2 on CTA pairs over pairs of row blocks of one expert; a
+    bias makes one expert hot (many blocks) and others small (a lone last block, paired
+    with rows that are computed and not stored)."""
     shape = wl.TINY
     x = wl.make_x(17, 1500, shape.H)
     bias = np.array([3.0, 0.0, -1.0, 0.5, -2.0, 1.0, 0.0, -0.5])
@@ -292,7 +293,7 @@ def test_paired_gemm1_with_odd_and_even_block_counts(oracle):
 
 # ------------------------------------------------- other sizes of the same layer family
 # Each case changes what the kernels tile over: a wider H and I (more k blocks and column
-# blocks), an I of 11 column blocks (odd, so GEMM 1 never pairs), H = 14 down-projection
+# blocks), an I of 11 column blocks (an odd count), H = 14 down-projection
 # tiles, 512 experts (the largest E the view accepts) with k = 10 (two combine groups), and
 # non-renormalised weights at the Qwen3.5-35B shape.
 SWEEP = {
