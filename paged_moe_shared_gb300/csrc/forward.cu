@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -41,15 +42,17 @@ std::string cuda_msg(const char* what, cudaError_t e) {
   return std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
 }
 
+// SM count per device, looked up once (callers may be on several threads).
 int sm_count_of(int device) {
-  static int cached_dev = -1, cached = 0;
-  if (device != cached_dev) {
-    int n = 0;
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cached[kMaxDevices];  // 0 = not looked up yet
+  if (device < 0 || device >= kMaxDevices) return 0;
+  int n = cached[device].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) n = 0;
-    cached = n;
-    cached_dev = device;
+    cached[device].store(n, std::memory_order_relaxed);
   }
-  return cached;
+  return n;
 }
 
 uint64_t align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }

@@ -23,6 +23,12 @@
 // columns) so the epilogue of one tile overlaps the main loop of the next.
 // Warp roles: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
 // warps 2-5 = epilogue (warp w reads TMEM lanes 32 * (w % 4) ..).
+// GEMM 1 past the small-batch size (kGatherA) has no x_sorted to read: warps
+// 6-9 copy each A stage's rows straight from x with cp.async, the producer
+// loads only the weight boxes, and the stage's full barrier also counts the
+// 128 loader threads.
+#include <atomic>
+
 #include "device.cuh"
 #include "kernels.h"
 
@@ -419,12 +425,17 @@ __global__ void __launch_bounds__(kGatherA ? kThreadsGather : kThreads, 1)
 template <bool kSwiGLU, bool kGatherA>
 cudaError_t launch_gemm(const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a,
                         const LaunchOpts& o) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t st = cudaFuncSetAttribute(paged_gemm_kernel<kSwiGLU, kGatherA>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  // the shared-memory opt-in is a per-device function attribute: set it once per device
+  static std::atomic<bool> configured[64];
+  int dev = 0;
+  cudaError_t st = cudaGetDevice(&dev);
+  if (st != cudaSuccess) return st;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev].load(std::memory_order_acquire)) {
+    st = cudaFuncSetAttribute(paged_gemm_kernel<kSwiGLU, kGatherA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemBytes);
     if (st != cudaSuccess) return st;
-    configured = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   const long long tiles = static_cast<long long>(a.max_tiles) * a.n_blocks * a.splits;
   const int grid = static_cast<int>(tiles < o.sm_count ? tiles : o.sm_count);

@@ -30,6 +30,8 @@
 //
 // Warps: 0 = TMA producer, 1 = TMEM allocation (both CTAs) and MMA issue
 // (rank 0), 2-5 = epilogue (warp w reads TMEM lanes 32 * (w % 4)).
+#include <atomic>
+
 #include "device.cuh"
 #include "kernels.h"
 
@@ -275,8 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 int max_pair_clusters(const LaunchOpts& o) {
-  static int cached = -1;
-  if (cached < 0) {
+  // per device (the kernel's occupancy depends on the GPU), looked up once
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cached[kMaxDevices];  // 0 = not looked up yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return o.sm_count / 2;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (o.sm_count / 2));
     cfg.blockDim = dim3(kThreads);
@@ -288,22 +295,28 @@ int max_pair_clusters(const LaunchOpts& o) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm2_kernel, &cfg) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm2_kernel, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
       n = o.sm_count / 2;
-    cached = n;
+    }
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached;
+  return n;
 }
 
 cudaError_t launch_pair(const CUtensorMap& tm_act, const CUtensorMap& tm_w, const GemmArgs& a,
                         const LaunchOpts& o) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t st = cudaFuncSetAttribute(pair_gemm2_kernel,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  // the shared-memory opt-in is a per-device function attribute: set it once per device
+  static std::atomic<bool> configured[64];
+  int dev = 0;
+  cudaError_t st = cudaGetDevice(&dev);
+  if (st != cudaSuccess) return st;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev].load(std::memory_order_acquire)) {
+    st = cudaFuncSetAttribute(pair_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemBytes);
     if (st != cudaSuccess) return st;
-    configured = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   const long long tiles = static_cast<long long>(a.max_tiles) * a.n_blocks;
   const int clusters_cap = max_pair_clusters(o);
