@@ -325,11 +325,11 @@ def run_ours(args, rank, world, local_rank):
     ws_ptr = (ws_raw.data_ptr() + 1023) // 1024 * 1024
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step(on=None):
         layer = counter[0] % n_layers
         counter[0] += 1
         R.rimuru_moe_forward(x.data_ptr(), logits.data_ptr(), w.T, ev, layer, out.data_ptr(),
-                             ws_ptr, ws_bytes, stream.cuda_stream)
+                             ws_ptr, ws_bytes, (on or stream).cuda_stream)
 
     def barrier():
         if dist is not None:
@@ -445,6 +445,36 @@ def run_ours(args, rank, world, local_rank):
             raise RuntimeError("host-buffer forward disagrees with the device-buffer forward")
     e2e_value = world * w.T * Ke / (ms_e2e / 1e3)
 
+    # ------------------------------------------------------------ CUDA-graph replay
+    # The same device-resident forwards recorded once by stream capture and replayed, as a
+    # decode loop with fixed buffers would run them (reported beside `value`, which
+    # launches every forward from the host).
+    G = max(n_layers, 10)
+    gs = torch.cuda.Stream(dev)
+    gs.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        for _ in range(G):
+            step(gs)
+    reps = max(1, K // G)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(gs):  # replay() launches on the current stream
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        barrier()
+        g0.record(gs)
+        for _ in range(reps):
+            graph.replay()
+        g1.record(gs)
+    torch.cuda.synchronize()
+    barrier()
+    ms_graph = max_over_ranks(g0.elapsed_time(g1), dist, dev)
+    if R.rimuru_get_device_error(ev) != R.DEV_OK:
+        raise RuntimeError("device error in the graph replays")
+    graph_value = world * w.T * reps * G / (ms_graph / 1e3)
+    del graph
+
     # ---------------------------------------------------------------- roofline
     peaks = load_peaks()
     # the binding roofline of the dominant kernel: whichever of its byte time and its
@@ -505,6 +535,9 @@ def run_ours(args, rank, world, local_rank):
                 "ms_per_step": round(ms_e2e / Ke, 5),
                 "api": "rimuru_moe_forward_host (pinned host buffers)", "streams": 2,
                 "single_stream_value": round(world * w.T * Ke / (ms_e2e_serial / 1e3), 1)},
+        "cuda_graph": {"value": round(graph_value, 1), "unit": "tokens/s",
+                       "ms_per_step": round(ms_graph / (reps * G), 5),
+                       "forwards_per_graph": G, "replays": reps},
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -286,6 +286,12 @@ int rimuru_moe_workspace_layout(rimuru_view_t view, int num_tokens, rimuru_ws_la
  * Every (layer, expert, projection) of `layer` must be mapped
  * (RIMURU_ERR_UNMAPPED otherwise).  Host-side checks run before any launch;
  * kernel-side problems set the device error word and never trap.
+ * CUDA graphs: the first forward after the view's mappings change copies the
+ * page table to the device and may wait for an earlier copy; any other
+ * forward only launches kernels on `stream` (with programmatic dependent
+ * launch), so it can be recorded by stream capture and replayed.  Replays use
+ * the pointers and the token count of the recorded call, and read the page
+ * table as it is on the device when they run.
  */
 int rimuru_moe_forward(const void* x_bf16, const float* logits, int num_tokens, rimuru_view_t view,
                        int layer, void* out_bf16, void* workspace, uint64_t workspace_bytes,

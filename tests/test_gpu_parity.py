@@ -359,3 +359,41 @@ def test_host_buffer_forward_equals_device_forward(oracle, pinned):
     finally:
         r.close()
     check(ref, w, run_oracle(oracle, w))
+
+
+def test_forward_replays_from_a_cuda_graph(oracle):
+    """A forward recorded by stream capture (after one plain forward has uploaded the page
+    table) replays to the same bits as plain forwards, including after the inputs change."""
+    import torch
+
+    from paged_moe_shared_gb300 import rimuru as R
+
+    w = wl.q35_mixed_pool(4, T=16)
+    r = Runner(w)
+    try:
+        s = torch.cuda.Stream()
+        r.forward(s)
+        s.synchronize()
+        plain = r.out.clone()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            r.forward(s)
+        r.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(r.out, plain)
+        # new inputs in the same buffers: the replay computes on them
+        w2 = wl.q35_mixed_pool(5, T=16)
+        r.x.copy_(torch.from_numpy(w2.x_bits.view(np.int16)).view(torch.bfloat16))
+        r.logits.copy_(torch.from_numpy(w2.logits))
+        g.replay()
+        torch.cuda.synchronize()
+        replayed = r.out.clone()
+        r.forward(s)
+        s.synchronize()
+        assert torch.equal(replayed, r.out)
+        assert R.rimuru_get_device_error(r.ev) == R.DEV_OK
+    finally:
+        r.close()
+    check(run_gpu(w), w, run_oracle(oracle, w))
+
