@@ -301,6 +301,9 @@ SWEEP = {
     "h2048_i1408_e60_k4_t300": (wl.MoEShape(H=2048, I=1408, E=60, k=4), 300, 24),
     "h3584_i2560_e16_k4_t40": (wl.MoEShape(H=3584, I=2560, E=16, k=4), 40, 12),
     "h1024_i256_e512_k10_t64": (wl.MoEShape(H=1024, I=256, E=512, k=10), 64, None),
+    # the largest top-k the kernels take (32 slots: one per lane) on both launch sequences
+    "h256_i128_e64_k32_t32": (wl.MoEShape(H=256, I=128, E=64, k=32), 32, None),
+    "h256_i128_e64_k32_t40": (wl.MoEShape(H=256, I=128, E=64, k=32), 40, None),
 }
 
 
