@@ -14,6 +14,11 @@ namespace {
 using dev::grid_dep_launch;
 using dev::grid_dep_wait;
 using dev::set_error;
+using dev::cluster_addr;
+using dev::cluster_id_x;
+using dev::cluster_rank;
+using dev::cluster_sync;
+using dev::ld_cluster_u32;
 
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -31,6 +36,27 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = o.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// The same with thread-block clusters of `cluster` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, int cluster,
+                           const LaunchOpts& o, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = o.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = o.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
@@ -268,15 +294,21 @@ __global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
 
 // ----------------------------------------------------- small batches, one launch
 // Route, align and gather in one kernel when all A = T * k assignments fit one
-// CTA (A <= kChunkAssign, decode-sized batches).  Every CTA routes all T tokens
-// and groups the assignments in shared memory: a few microseconds of repeated
-// work per CTA instead of two kernel boundaries and the global round trip of
-// the routing tables.  CTA 0 writes ids, weights, offsets, sorted, inv and the
-// tile tables; every CTA copies its share of the rows into x_sorted.
+// CTA (A <= kChunkAssign, decode-sized batches).  CTAs come in clusters of
+// kFusedCluster: the CTA of rank r routes the tokens t = r (mod kFusedCluster)
+// and, after a cluster barrier, every CTA copies the others' expert ids out of
+// their shared memory, so each cluster holds the whole routing without a
+// grid-wide step and each SM routes an eighth of the tokens.  Every CTA then
+// groups the assignments in shared memory: a few microseconds of repeated work
+// per CTA instead of two kernel boundaries and the global round trip of the
+// routing tables.  Cluster 0 writes ids and weights (each CTA its own
+// tokens), CTA 0 offsets, sorted, inv and the tile tables; every CTA copies its
+// share of the rows into x_sorted.
 // Grouping: assignment f = 32 g + lane belongs to warp g; within the warp its
 // rank among equal experts comes from __match_any_sync, across warps from a
 // prefix over per-warp counts, so the order is f ascending inside each expert.
 constexpr int kFusedWarps = kChunkAssign / 32;
+constexpr int kFusedCluster = 8;
 
 template <int EPL>
 __global__ void __launch_bounds__(kChunkAssign) moe_route_align_gather_kernel(
@@ -297,20 +329,28 @@ __global__ void __launch_bounds__(kChunkAssign) moe_route_align_gather_kernel(
   const int A = T * k;
   const int groups = (A + 31) / 32;
   const bool lead = blockIdx.x == 0;
+  const uint32_t crank = cluster_rank();
+  const bool lead_cluster = cluster_id_x() == 0;
   for (int i = tid; i < groups * kMaxExperts; i += blockDim.x) (&s_wh[0][0])[i] = 0;
-  for (int t = warp; t < T; t += kFusedWarps) {
+  for (int t = static_cast<int>(crank) + kFusedCluster * warp; t < T;
+       t += kFusedCluster * kFusedWarps) {
     int my_id;
     float my_w;
     route_token<EPL>(logits + static_cast<size_t>(t) * E, E, k, renorm, lane, err, my_id, my_w);
     if (lane < k) {
       s_ids[t * k + lane] = my_id;
-      if (lead) {
+      if (lead_cluster) {
         ids[t * k + lane] = my_id;
         w[t * k + lane] = my_w;
       }
     }
   }
-  __syncthreads();
+  cluster_sync();  // every CTA's routed ids are in its shared memory
+  if (tid < A) {
+    const uint32_t owner = static_cast<uint32_t>((tid / k) % kFusedCluster);
+    if (owner != crank) s_ids[tid] = static_cast<int>(ld_cluster_u32(cluster_addr(&s_ids[tid], owner)));
+  }
+  cluster_sync();  // no CTA leaves or moves on while a peer still reads its ids
   const int f = warp * 32 + lane;
   const unsigned valid = __ballot_sync(kFull, f < A);
   int my_e = 0, rank_in = 0;
@@ -454,25 +494,26 @@ cudaError_t launch_route_align_gather(const float* logits, const __nv_bfloat16* 
                                       int32_t* num_ptiles, int32_t* tile_cnt, int cnt_len,
                                       __nv_bfloat16* x_sorted, int* err, const LaunchOpts& o) {
   const int A = T * k;
-  const int grid = max(1, min((A + kFusedRowsPerCta - 1) / kFusedRowsPerCta, o.sm_count));
+  int grid = max(1, min((A + kFusedRowsPerCta - 1) / kFusedRowsPerCta, o.sm_count));
+  grid = (grid + kFusedCluster - 1) / kFusedCluster * kFusedCluster;  // whole clusters
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   uint4* xsv = reinterpret_cast<uint4*>(x_sorted);
   const dim3 g(grid), b(kChunkAssign);
   if (E <= 32)
-    return launch(moe_route_align_gather_kernel<1>, g, b, 0, o, logits, xv, T, E, k, renorm, H / 8,
-                  ids, w, offsets, sorted, inv, tiles, num_tiles, ptiles, num_ptiles, tile_cnt,
-                  cnt_len, xsv, err);
+    return launch_cluster(moe_route_align_gather_kernel<1>, g, b, kFusedCluster, o, logits, xv, T,
+                          E, k, renorm, H / 8, ids, w, offsets, sorted, inv, tiles, num_tiles,
+                          ptiles, num_ptiles, tile_cnt, cnt_len, xsv, err);
   if (E <= 128)
-    return launch(moe_route_align_gather_kernel<4>, g, b, 0, o, logits, xv, T, E, k, renorm, H / 8,
-                  ids, w, offsets, sorted, inv, tiles, num_tiles, ptiles, num_ptiles, tile_cnt,
-                  cnt_len, xsv, err);
+    return launch_cluster(moe_route_align_gather_kernel<4>, g, b, kFusedCluster, o, logits, xv, T,
+                          E, k, renorm, H / 8, ids, w, offsets, sorted, inv, tiles, num_tiles,
+                          ptiles, num_ptiles, tile_cnt, cnt_len, xsv, err);
   if (E <= 256)
-    return launch(moe_route_align_gather_kernel<8>, g, b, 0, o, logits, xv, T, E, k, renorm, H / 8,
-                  ids, w, offsets, sorted, inv, tiles, num_tiles, ptiles, num_ptiles, tile_cnt,
-                  cnt_len, xsv, err);
-  return launch(moe_route_align_gather_kernel<16>, g, b, 0, o, logits, xv, T, E, k, renorm, H / 8,
-                ids, w, offsets, sorted, inv, tiles, num_tiles, ptiles, num_ptiles, tile_cnt,
-                cnt_len, xsv, err);
+    return launch_cluster(moe_route_align_gather_kernel<8>, g, b, kFusedCluster, o, logits, xv, T,
+                          E, k, renorm, H / 8, ids, w, offsets, sorted, inv, tiles, num_tiles,
+                          ptiles, num_ptiles, tile_cnt, cnt_len, xsv, err);
+  return launch_cluster(moe_route_align_gather_kernel<16>, g, b, kFusedCluster, o, logits, xv, T,
+                        E, k, renorm, H / 8, ids, w, offsets, sorted, inv, tiles, num_tiles,
+                        ptiles, num_ptiles, tile_cnt, cnt_len, xsv, err);
 }
 
 cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv, const float* w, int T,
