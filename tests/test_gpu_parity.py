@@ -400,3 +400,23 @@ def test_forward_replays_from_a_cuda_graph(oracle):
         r.close()
     check(run_gpu(w), w, run_oracle(oracle, w))
 
+
+
+def test_sampled_profiling_records_every_nth_forward():
+    """rimuru_profile_enable_sampled(every = 3, capacity = 4) over ten forwards brackets the
+    selected kernel in forwards 0, 3, 6 and 9 only; kernels not selected report nothing."""
+    from paged_moe_shared_gb300 import rimuru as R
+
+    w = wl.tiny(3, T=16)
+    r = Runner(w)
+    try:
+        R.rimuru_profile_enable_sampled(r.ev, 1 << R.K_GEMM1, 4, 3)
+        for _ in range(10):
+            r.forward()
+        n, ms = R.rimuru_profile_read(r.ev, R.K_GEMM1)
+        assert n == 4 and ms > 0
+        assert R.rimuru_profile_read(r.ev, R.K_GEMM2) == (0, 0.0)
+        R.rimuru_profile_enable(r.ev, 0, 1)
+        assert R.rimuru_get_device_error(r.ev) == R.DEV_OK
+    finally:
+        r.close()
