@@ -33,6 +33,13 @@ MUTANTS = {
     "page_offset": [("uint64_t start = (uint64_t)page_id * page_bytes;",
                      "uint64_t start = (uint64_t)page_id * page_bytes + 2;")],
     "gate_bias_in_silu": [("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(-u[i])) * u[i];")],
+    "bf16_subnormal_scale": [("ldexp((double)frac, -126 - 7)", "ldexp((double)frac, -126 - 8)")],
+    "bf16_exponent_bias": [("ldexp(1.0 + (double)frac / 128.0, expo - 127)",
+                            "ldexp(1.0 + (double)frac / 128.0, expo - 126)")],
+    "full_softmax_skips_expert0": [("for (int e = 0; e < E; ++e) sum_all +=",
+                                    "for (int e = 1; e < E; ++e) sum_all +=")],
+    "topk_ascending_values": [("if (l[a] > l[b]) return 1;\n  if (l[a] < l[b]) return 0;",
+                               "if (l[a] < l[b]) return 1;\n  if (l[a] > l[b]) return 0;")],
 }
 
 
