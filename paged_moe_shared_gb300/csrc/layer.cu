@@ -151,8 +151,8 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   const LayerPtrs q = pointers_of(a);
   const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I;
   const int A = T * k;
-  CUtensorMap tm_x, tm_h;
-  {
+  CUtensorMap tm_x{}, tm_h;
+  if (gathered) {  // x_sorted exists (and is read by GEMM 1) only behind the small-batch kernel
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(A)};
     cuuint64_t str[1] = {static_cast<cuuint64_t>(H) * 2};
     cuuint32_t box[2] = {64, 128};
