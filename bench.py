@@ -201,6 +201,8 @@ def run_offload(args, rank, world, local_rank):
     ev = pool.view(pb)
     R.rimuru_view_set_moe_shape(ev, L, E, H, I, shape.k, shape.renorm)
     off = R.rimuru_offload_create(ev, host.data_ptr(), cap, 0)
+    policy = R.EVICT_LAYER_CYCLE if args.evict == "layer_cycle" else R.EVICT_LRU
+    R.rimuru_offload_set_policy(off, policy)
     xs = [torch.from_numpy(st.x_bits[0][i].view(np.int16)).view(torch.bfloat16).to(dev)
           for i in range(8)]
     lgs = [torch.from_numpy(st.logits[0][i]).to(dev) for i in range(8)]
@@ -261,7 +263,7 @@ def run_offload(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(ms / K, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"q3_stack_offload: {WORKLOAD_TEXT['q3_stack_offload']}",
-                   "layers": L, "tokens": T, "resident_experts": cap,
+                   "layers": L, "tokens": T, "resident_experts": cap, "eviction": args.evict,
                    "host_pages_gib": round(host.numel() / 2**30, 1),
                    "l2": "inputs larger than L2 (the stack reads 54 GiB of expert pages)"},
         "roofline": {"bound": "h2d", "achieved": round(achieved, 1), "peak": round(link_gbs, 1),
@@ -630,6 +632,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--evict", default="layer_cycle", choices=["layer_cycle", "lru"],
+                    help="eviction policy of the offload cache (q3_stack_offload)")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = REF_DEFAULT_STEPS if args.impl == "reference" else DEFAULT_STEPS[args.workload]

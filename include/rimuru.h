@@ -423,6 +423,23 @@ int rimuru_offload_forward(rimuru_offload_t off, const void* x_bf16, const float
 
 int rimuru_offload_stats(rimuru_offload_t off, rimuru_offload_counters* out);
 
+/* Eviction policy of the cache (the pages name none).
+ *   RIMURU_EVICT_LRU          least recently used slot (the default).
+ *   RIMURU_EVICT_LAYER_CYCLE  for stacks whose layers run in order 0, 1, ...,
+ *                             L-1, 0, ... (every decode step of a model): the
+ *                             slot whose expert's layer comes last counting on
+ *                             from the next forward's layer (the layer after
+ *                             the last forward, or that forward's own layer
+ *                             while it loads), i.e. whose next use is furthest
+ *                             away; empty slots first, ties to the least
+ *                             recently used.  Where a cycle of layers does not
+ *                             fit, LRU misses on every expert; this keeps a
+ *                             fixed part of the cycle resident.
+ * Slots claimed by the current prefetch or forward are never victims under
+ * either policy.  Errors: RIMURU_ERR_ARG (null handle, unknown policy). */
+enum { RIMURU_EVICT_LRU = 0, RIMURU_EVICT_LAYER_CYCLE = 1 };
+int rimuru_offload_set_policy(rimuru_offload_t off, int policy);
+
 /* Change the number of resident experts.  Shrinking waits (on the host) for
  * the cache's copies and for the last forward it recorded, evicts the least
  * recently used slots and frees their pages (the allocator merges them back

@@ -63,6 +63,8 @@ struct Offload {
   std::vector<int> prv, nxt;       // LRU list over slots; head = most recent
   int head = -1, tail = -1;
   int64_t op = 0, seq = 0;
+  int policy = RIMURU_EVICT_LRU;
+  int next_layer = 0;  // layer the next forward is expected to run (layer-cycle policy)
 
   std::vector<cudaEvent_t> done_ev;   // [kDoneRing]
   std::vector<cudaEvent_t> ready_ev;  // [L]
@@ -127,6 +129,32 @@ struct Offload {
     v->table_dirty = true;
   }
 
+  // The slot to refill, never one claimed by the current operation.
+  //  LRU: the least recently used.
+  //  Layer cycle (layers run 0, 1, ..., L-1, 0, ... as in every decode step of
+  //  a model): the slot whose expert's layer comes last counting on from the
+  //  next forward's layer, i.e. whose next use is furthest away (Belady's rule
+  //  for a cyclic order); empty slots first, ties to the least recently used.
+  //  Under LRU a cycle of L layers larger than the cache misses on every
+  //  expert; this keeps a fixed part of the cycle resident.
+  int victim() const {
+    if (policy == RIMURU_EVICT_LRU) {
+      int s = tail;
+      while (s >= 0 && slot_op[s] == op) s = prv[s];
+      return s;
+    }
+    int best = -1, best_d = -1;
+    for (int s = tail; s >= 0; s = prv[s]) {
+      if (slot_op[s] == op) continue;
+      const int d = slot_key[s] < 0 ? L : ((slot_key[s] / E - next_layer) % L + L) % L;
+      if (d > best_d) {
+        best = s;
+        best_d = d;
+      }
+    }
+    return best;
+  }
+
   // Make expert (layer, e) resident; `protect` slots claimed in this operation.
   int load(int layer, int e, bool demand, bool* was_hit) {
     const int key = layer * E + e;
@@ -138,8 +166,7 @@ struct Offload {
       return RIMURU_OK;
     }
     *was_hit = false;
-    s = tail;
-    while (s >= 0 && slot_op[s] == op) s = prv[s];
+    s = victim();
     if (s < 0)
       return fail(RIMURU_ERR_OOM, "offload capacity is smaller than the experts one layer needs");
     const int old = slot_key[s];
@@ -463,6 +490,7 @@ int rimuru_offload_forward(rimuru_offload_t off, const void* x_bf16, const float
 
   // 2. every routed expert resident (demand copies for the misses)
   o.op += 1;
+  o.next_layer = layer;
   std::vector<int> routed;
   routed.reserve(o.E);
   for (int ex = 0; ex < o.E; ++ex)
@@ -506,6 +534,16 @@ int rimuru_offload_forward(rimuru_offload_t off, const void* x_bf16, const float
   if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, rimuru::cuda_msg("completion event", e));
   for (int ex : routed) o.slot_seq[o.key_slot[layer * o.E + ex]] = o.seq;
   o.st.forwards += 1;
+  o.next_layer = (layer + 1) % o.L;
+  return RIMURU_OK;
+}
+
+int rimuru_offload_set_policy(rimuru_offload_t off, int policy) {
+  rimuru::clear_error();
+  if (!off) return fail(RIMURU_ERR_ARG, "null handle");
+  if (policy != RIMURU_EVICT_LRU && policy != RIMURU_EVICT_LAYER_CYCLE)
+    return fail(RIMURU_ERR_ARG, "unknown eviction policy");
+  off->o.policy = policy;
   return RIMURU_OK;
 }
 

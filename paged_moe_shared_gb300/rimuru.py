@@ -44,6 +44,7 @@ EXPORTS = [
     "rimuru_profile_read", "rimuru_device_sm_count", "rimuru_selftest_bounded_wait",
     "rimuru_offload_create", "rimuru_offload_destroy", "rimuru_offload_prefetch",
     "rimuru_offload_forward", "rimuru_offload_stats", "rimuru_offload_resident",
+    "rimuru_offload_set_policy",
     "rimuru_page_alloc_near", "rimuru_pool_fragmentation", "rimuru_offload_resize",
     "rimuru_offload_capacity", "rimuru_adjust",
 ]
@@ -116,6 +117,7 @@ def _load():
         "rimuru_offload_prefetch": ([P, i32, P, i32], i32),
         "rimuru_offload_forward": ([P, P, P, i32, i32, P, P, u64, P], i32),
         "rimuru_offload_stats": ([P, ctypes.POINTER(OffloadCounters)], i32),
+        "rimuru_offload_set_policy": ([P, i32], i32),
         "rimuru_offload_resident": ([P, i32, i32, ctypes.POINTER(i32)], i32),
         "rimuru_offload_resize": ([P, i32], i32),
         "rimuru_offload_capacity": ([P, ctypes.POINTER(i32)], i32),
@@ -353,6 +355,14 @@ def rimuru_offload_forward(off, x_ptr: int, logits_ptr: int, num_tokens: int, la
                                       num_tokens, layer, ctypes.c_void_p(out_ptr),
                                       ctypes.c_void_p(workspace_ptr), workspace_bytes,
                                       ctypes.c_void_p(stream)))
+
+
+EVICT_LRU, EVICT_LAYER_CYCLE = 0, 1
+
+
+def rimuru_offload_set_policy(off, policy: int) -> None:
+    """Eviction policy of the offload cache: EVICT_LRU (default) or EVICT_LAYER_CYCLE."""
+    _check(lib.rimuru_offload_set_policy(off, policy))
 
 
 def rimuru_offload_stats(off) -> dict:

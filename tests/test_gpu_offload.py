@@ -3,7 +3,8 @@ prefetch and eviction counts against an independent model of the policy (least r
 used slot first; slots claimed by the same prefetch or forward are never evicted by it).
 
 Rimuru page: experts kept in CPU memory with a device cache (Figure 1 panel b) and dual
-buffers that overlap prefetch with execution (Figure 8)."""
+buffers that overlap prefetch with execution (Figure 8).  The eviction policy is this
+library's (the pages name none): least recently used, or the layer-cycle rule."""
 from __future__ import annotations
 
 import numpy as np
@@ -20,16 +21,37 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-class LRUModel:
-    """Slots in recency order (index 0 = most recent); initially slot 0 is the oldest."""
+class CacheModel:
+    """Slots in recency order (index 0 = most recent); initially slot 0 is the oldest.
+    Victims: the least recently used slot (LRU), or the slot whose layer comes last counting
+    on from the next forward's layer (layer cycle), empty slots first, ties to the least
+    recently used; never a slot claimed by the current operation."""
 
-    def __init__(self, cap):
+    def __init__(self, cap, policy=R.EVICT_LRU, L=1, E=1):
         self.order = list(range(cap - 1, -1, -1))
         self.slot_key = [None] * cap
         self.key_slot = {}
         self.claimed = {}
         self.op = 0
+        self.policy, self.L, self.E = policy, L, E
+        self.next_layer = 0
         self.c = dict(hits=0, misses=0, prefetch_loads=0, evictions=0, bytes_h2d=0, forwards=0)
+
+    def _victim(self):
+        free = [s for s in reversed(self.order) if self.claimed.get(s) != self.op]
+        if not free:
+            raise AssertionError("capacity too small")
+        if self.policy == R.EVICT_LRU:
+            return free[0]
+
+        def dist(s):
+            k = self.slot_key[s]
+            return self.L if k is None else (k // self.E - self.next_layer) % self.L
+        best = free[0]
+        for s in free[1:]:
+            if dist(s) > dist(best):
+                best = s
+        return best
 
     def _load(self, key, demand, nbytes):
         s = self.key_slot.get(key)
@@ -38,11 +60,7 @@ class LRUModel:
             self.order.insert(0, s)
             self.claimed[s] = self.op
             return True
-        for s in reversed(self.order):
-            if self.claimed.get(s) != self.op:
-                break
-        else:
-            raise AssertionError("capacity too small")
+        s = self._victim()
         old = self.slot_key[s]
         if old is not None:
             del self.key_slot[old]
@@ -62,15 +80,17 @@ class LRUModel:
         for k in keys:
             self._load(k, False, nbytes)
 
-    def forward(self, keys, nbytes):
+    def forward(self, layer, keys, nbytes):
         self.op += 1
+        self.next_layer = layer
         for k in keys:
             hit = self._load(k, True, nbytes)
             self.c["hits" if hit else "misses"] += 1
         self.c["forwards"] += 1
+        self.next_layer = (layer + 1) % self.L
 
 
-def run_stack(st: wl.OffloadStack, cap: int, prefetch: bool):
+def run_stack(st: wl.OffloadStack, cap: int, prefetch: bool, policy=R.EVICT_LRU):
     s = st.shape
     E = s.E
     pb = st.page_bytes
@@ -81,7 +101,8 @@ def run_stack(st: wl.OffloadStack, cap: int, prefetch: bool):
     R.rimuru_view_set_moe_shape(ev, st.L, E, s.H, s.I, s.k, s.renorm)
     pool.upload(wl.empty_pool((3 * cap + 5) * pb))
     off = R.rimuru_offload_create(ev, host.data_ptr(), cap, 0)
-    model = LRUModel(cap)
+    R.rimuru_offload_set_policy(off, policy)
+    model = CacheModel(cap, policy, st.L, E)
     nbytes = 3 * s.H * s.I * 2
     ws_bytes = R.rimuru_moe_workspace_bytes(ev, st.T)
     ws_raw = torch.empty(ws_bytes + 1024, dtype=torch.uint8, device=DEV)
@@ -104,7 +125,7 @@ def run_stack(st: wl.OffloadStack, cap: int, prefetch: bool):
                 out = torch.empty_like(x)
                 R.rimuru_offload_forward(off, x.data_ptr(), lg.data_ptr(), st.T, l, out.data_ptr(),
                                          ws_ptr, ws_bytes, stream)
-                model.forward([l * E + e for e in routed], nbytes)
+                model.forward(l, [l * E + e for e in routed], nbytes)
                 torch.cuda.synchronize()
                 assert R.rimuru_get_device_error(ev, clear=True) == R.DEV_OK
                 err = rel_err(to_f64(out), o["out"])
@@ -135,6 +156,20 @@ def test_offloaded_stack_matches_oracle_and_lru_model(prefetch, cap):
         assert counters["prefetch_loads"] > 0
     if cap == 20:
         assert counters["hits"] > 0
+
+
+@pytest.mark.parametrize("prefetch", [False, True], ids=["demand_only", "prefetch"])
+def test_layer_cycle_policy_keeps_part_of_the_cycle_resident(prefetch):
+    """The same stack over 4 steps with the layer-cycle policy: outputs against the oracle,
+    counters against the model, and fewer host-to-device bytes than LRU, which misses on
+    every expert of a cycle larger than the cache."""
+    shape = wl.MoEShape(H=256, I=128, E=8, k=2)
+    st = wl.offload_stack(shape, L=6, T=16, steps=4, seed=53)
+    cyc, cyc_model, _ = run_stack(st, cap=24, prefetch=prefetch, policy=R.EVICT_LAYER_CYCLE)
+    assert cyc == cyc_model
+    lru, lru_model, _ = run_stack(st, cap=24, prefetch=prefetch, policy=R.EVICT_LRU)
+    assert lru == lru_model
+    assert cyc["bytes_h2d"] < lru["bytes_h2d"] and cyc["hits"] >= lru["hits"]
 
 
 def test_capacity_below_one_layer_is_rejected():
