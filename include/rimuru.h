@@ -371,8 +371,9 @@ int rimuru_moe_forward_noalloc(const void* x_bf16, const float* logits, int num_
  * expert of every layer lives in pinned host memory; `capacity_experts` of
  * them are resident at a time, each in three pages of the expert view that
  * the cache allocates at creation.  A miss is copied host -> device on the
- * copy stream straight into the pages of the least recently used slot
- * (this library's choice: the pages name no eviction policy).
+ * copy stream straight into the pages of the slot the eviction policy picks
+ * (least recently used unless rimuru_offload_set_policy chooses otherwise;
+ * the pages name no eviction policy).
  *
  * host_pages  pinned host memory (cudaHostAlloc or registered) holding
  *             layers * experts * 3 pages of the view's page size; projection
@@ -405,7 +406,7 @@ int rimuru_offload_create(rimuru_view_t view, const void* host_pages, int capaci
 int rimuru_offload_destroy(rimuru_offload_t off);
 
 /* Queue copies on the copy stream that make the listed experts (host array
- * of n expert ids) of `layer` resident, evicting least recently used ones.
+ * of n expert ids) of `layer` resident, evicting by the cache's policy.
  * Returns at once; call it for layer l + 1 before the forward of layer l so
  * the copies overlap that layer's kernels. */
 int rimuru_offload_prefetch(rimuru_offload_t off, int layer, const int32_t* experts, int n);
