@@ -98,6 +98,8 @@ struct GemmArgs {
 };
 
 // a3: h = silu(x_sorted w1_e) * (x_sorted w3_e); w1/w3 read in place from pages.
+// A is staged by TMA from x_sorted, which the fused small-batch kernel writes
+// (batches of at most kChunkAssign assignments).
 cudaError_t launch_gemm1_swiglu(const CUtensorMap& tm_x, const CUtensorMap& tm_w13,
                                 const GemmArgs& a, const LaunchOpts& o);
 // Use the CTA-pair GEMM 2 when the assignments average at least this many
