@@ -109,6 +109,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// L2 prefetch of one box of a 3-D tiled tensor map: no shared memory, no
+// barrier, nothing to wait for.  Coordinates past the tensor read nothing.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(m),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // ------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy through the L1-bypassing path (generic proxy).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {

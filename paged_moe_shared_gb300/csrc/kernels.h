@@ -15,6 +15,8 @@ constexpr int kRouteWarps = 32;     // tokens per routing chunk: one warp per to
 constexpr int kTileM = 128;         // rows (assignments) per GEMM tile
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
+// k blocks of weights (32 KiB each) a GEMM CTA prefetches into L2 ahead of its first tile.
+constexpr int kPrefetchKBlocks = 16;
 
 // Split-K for layers with few tiles: the K range of a tile is cut into S
 // parts computed by different CTAs (fp32 partials in the workspace, summed
@@ -95,6 +97,12 @@ struct GemmArgs {
   const int32_t* sorted;      // [A]
   int top_k;
   int ldx;
+  // Weight prefetch before the grid dependency wait: the CTA guesses its first
+  // tile's expert as if every expert had prefetch_bpe row blocks and prefetches
+  // the first prefetch_kb k blocks of that tile's weights into L2 (0: off).
+  int prefetch_kb;
+  int prefetch_bpe;
+  int num_experts;
 };
 
 // a3: h = silu(x_sorted w1_e) * (x_sorted w3_e); w1/w3 read in place from pages.

@@ -121,7 +121,10 @@ int launch_layer_route(const LayerLaunch& a) {
   LaunchOpts first;
   first.stream = a.stream;
   first.sm_count = a.sm_count;
-  first.pdl = false;  // the first kernel follows whatever the caller queued
+  // The first kernel may be scheduled while the caller's last kernel drains:
+  // it runs griddepcontrol.wait before touching any data, which waits for that
+  // kernel's completion and memory flush (and is a no-op behind non-kernel work).
+  first.pdl = a.pdl;
   LaunchOpts next = first;
   next.pdl = a.pdl;
   cudaError_t e = cudaSuccess;
@@ -195,6 +198,15 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   g2.ldo = H;
   g2.n_blocks = H / 256;
   g2.num_k_blocks = I / 64;
+  // Weight-bound batches (at most half a 128-row block per expert on average,
+  // so the guessed first tiles mostly are the real ones) prefetch their first
+  // weight tile into L2 while the kernel before them finishes; larger batches
+  // reuse weights from L2 or would prefetch the wrong experts.
+  if (2LL * A <= static_cast<long long>(E) * kTileM) {
+    g1.prefetch_kb = g2.prefetch_kb = kPrefetchKBlocks;
+    g1.prefetch_bpe = g2.prefetch_bpe = 1;
+  }
+  g1.num_experts = g2.num_experts = E;
 
   LaunchOpts o;
   o.stream = a.stream;
@@ -253,7 +265,10 @@ int launch_layer(const LayerLaunch& a) {
   LaunchOpts first;
   first.stream = a.stream;
   first.sm_count = a.sm_count;
-  first.pdl = false;  // the first kernel follows whatever the caller queued
+  // The first kernel may be scheduled while the caller's last kernel drains:
+  // it runs griddepcontrol.wait before touching any data, which waits for that
+  // kernel's completion and memory flush (and is a no-op behind non-kernel work).
+  first.pdl = a.pdl;
   cudaError_t e = cudaSuccess;
   const int kidx = RIMURU_K_ROUTE_ALIGN_GATHER;
   const bool prof = a.ev && (a.ev_mask >> kidx & 1u);

@@ -107,6 +107,35 @@ __global__ void __launch_bounds__(kGatherA ? kThreadsGather : kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
 
+  if (threadIdx.x == 0 && p.prefetch_kb > 0) {
+    // Weights do not depend on the kernel we follow (only which experts are
+    // used does): start streaming the guessed first tile's weights into L2
+    // while that kernel still runs.  A wrong guess costs bandwidth only.
+    const int S = p.splits, nkb = p.num_k_blocks;
+    const int tile = blockIdx.x / S, split = blockIdx.x - tile * S;
+    const int e = tile / p.n_blocks / p.prefetch_bpe, nb = tile % p.n_blocks;
+    const int kb0 = split * nkb / S;
+    const int kb1 = min(kb0 + p.prefetch_kb, (split + 1) * nkb / S);
+    if (e < p.num_experts) {
+      const int pg0 = p.page_table[3 * e + (kSwiGLU ? RIMURU_PROJ_W1 : RIMURU_PROJ_W2)];
+      const int pg1 = kSwiGLU ? p.page_table[3 * e + RIMURU_PROJ_W3] : pg0;
+      if (pg0 >= 0 && pg0 < p.num_pages && pg1 >= 0 && pg1 < p.num_pages) {
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (kSwiGLU) {
+            const int n0 = nb * (BN / 2);
+            tma_prefetch_3d(&tm_w, n0, kb * BK, pg0);
+            tma_prefetch_3d(&tm_w, n0 + 64, kb * BK, pg0);
+            tma_prefetch_3d(&tm_w, n0, kb * BK, pg1);
+            tma_prefetch_3d(&tm_w, n0 + 64, kb * BK, pg1);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tma_prefetch_3d(&tm_w, nb * BN + 64 * c, kb * BK, pg0);
+          }
+        }
+      }
+    }
+  }
+
   grid_dep_wait();  // tile table, offsets and activations come from earlier kernels
   grid_dep_launch();  // the next kernel may be scheduled now; it waits for our completion
   const int S = p.splits;
