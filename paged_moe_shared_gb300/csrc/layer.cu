@@ -198,11 +198,13 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   g2.ldo = H;
   g2.n_blocks = H / 256;
   g2.num_k_blocks = I / 64;
-  // Weight-bound batches (at most half a 128-row block per expert on average,
-  // so the guessed first tiles mostly are the real ones) prefetch their first
-  // weight tile into L2 while the kernel before them finishes; larger batches
-  // reuse weights from L2 or would prefetch the wrong experts.
-  if (2LL * A <= static_cast<long long>(E) * kTileM) {
+  // Weight-bound batches prefetch their first weight tile into L2 while the
+  // kernel before them finishes.  The guess (tile i's expert = i / n_blocks)
+  // holds when nearly every expert is touched (at least two assignments per
+  // expert on average: about 86 % of the experts or more) and none has a second
+  // row block (at most half a block per expert on average); larger batches
+  // reuse weights from L2, smaller ones would prefetch the wrong experts.
+  if (A >= 2 * E && 2LL * A <= static_cast<long long>(E) * kTileM) {
     g1.prefetch_kb = g2.prefetch_kb = kPrefetchKBlocks;
     g1.prefetch_bpe = g2.prefetch_bpe = 1;
   }
