@@ -126,6 +126,7 @@ def source_digest(*rel_paths):
 
 GEMM_SOURCES = ("paged_moe_shared_gb300/csrc/moe_gemm.cu",
                 "paged_moe_shared_gb300/csrc/moe_gemm_2sm.cu",
+                "paged_moe_shared_gb300/csrc/moe_gemm_wide.cu",
                 "paged_moe_shared_gb300/csrc/device.cuh")
 
 

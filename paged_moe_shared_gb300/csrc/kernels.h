@@ -119,6 +119,12 @@ constexpr int kPairMinBlocksPerExpert = 2;
 cudaError_t launch_gemm1_swiglu_gather(const CUtensorMap& tm_w13, const GemmArgs& a,
                                        const LaunchOpts& o);
 
+// a3 for large batches (the same condition as the CTA-pair GEMM 2): 256-row
+// tiles of the pair table (tiles/num_tiles in `a` name it) on one SM, two
+// M = 128 MMAs per k step sharing the staged weights, A rows gathered from x
+// like launch_gemm1_swiglu_gather.  No split-K.
+cudaError_t launch_gemm1_wide(const CUtensorMap& tm_w13, const GemmArgs& a, const LaunchOpts& o);
+
 // a4 for large batches on CTA pairs (tcgen05 cta_group::2): a tile is one
 // entry of the pair table (tiles/num_tiles in `a` name it) times one column
 // block; each CTA stages half of every weight tile.

@@ -234,10 +234,16 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   if (e == cudaSuccess) {
     LaunchOpts o1 = o;
     o1.pdl = after_route && a.pdl;  // behind align or the small-batch kernel; not behind host work
-    if (gathered)
+    if (gathered) {
       e = launch_gemm1_swiglu(tm_x, *a.tm_w13, g1, o1);
-    else
+    } else if (pairs && sp.s1 == 1) {
+      GemmArgs w1 = g1;  // 256-row tiles from the pair table
+      w1.tiles = q.ptiles;
+      w1.num_tiles = q.num_ptiles;
+      e = launch_gemm1_wide(*a.tm_w13, w1, o1);
+    } else {
       e = launch_gemm1_swiglu_gather(*a.tm_w13, g1, o1);
+    }
   }
   mark(RIMURU_K_GEMM1, 1);
   mark(RIMURU_K_GEMM2, 0);
