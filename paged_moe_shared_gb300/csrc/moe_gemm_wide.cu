@@ -51,7 +51,11 @@ constexpr int kLoaderWarps = 4;
 constexpr int kFirstLoader = 2 + kEpiWarps;
 constexpr int kThreads = 32 * (kFirstLoader + kLoaderWarps);  // 448
 constexpr int kTmemCols = 2 * BN;            // the two halves' accumulators
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align slack*/ + 256 /*barriers*/;
+// Epilogue staging: per epilogue warp one 32-row x 128-byte block of h, 16-byte
+// chunks XOR-swizzled by row, so each store instruction writes four whole rows.
+constexpr int kStageOutBytes = 32 * 128;
+constexpr int kSmemBytes = kStages * kStageBytes + kEpiWarps * kStageOutBytes +
+                           1024 /*align slack*/ + 256 /*barriers*/;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 static_assert(kThreads * 128 <= 65536, "registers: 128 per thread fit one SM");
 
@@ -77,7 +81,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;                        // [stage][256 rows][128 B], 128-byte swizzle
   uint8_t* sB = smem + kStages * kABytes;    // [stage][4 chunks][64 k rows][128 B]
-  Shared* sh = reinterpret_cast<Shared*>(smem + kStages * kStageBytes);
+  uint8_t* sOut = smem + kStages * kStageBytes;  // [epilogue warp][32 rows][128 B]
+  Shared* sh = reinterpret_cast<Shared*>(sOut + kEpiWarps * kStageOutBytes);
   volatile int* abort = &sh->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -256,8 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_wait_all();  // no copy of this thread is in flight when the CTA exits
   } else {
     // -------------------------------------------------------------- epilogue
+    // Each warp turns its 32 rows x 64 columns of h into bf16 in registers,
+    // releases the accumulator half (the next tile's MMAs may start on it),
+    // then writes the rows out through its staging block.
     const int q = warp & 3;                  // TMEM lane quadrant this warp may read
     const int cb = 64 * ((warp - 2) >> 2);   // this warp's first output column of the block
+    const uint32_t blk_s = smem_u32(sOut + (warp - 2) * kStageOutBytes);
     uint32_t local = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++local) {
       const bool got = mbar_wait(&sh->tfull, local & 1u, abort);
@@ -273,36 +282,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         const int rows = min(BM, rem - h * BM);  // warp-uniform
+        uint32_t packed[32];
         if (rows > 0) {
-          const int r = q * 32 + lane;
-          const bool valid = r < rows;
-          __nv_bfloat16* orow = p.out + static_cast<size_t>(row0 + h * BM + r) * p.ldo + n0;
           const uint32_t tb = tmem_base + h * BN + (static_cast<uint32_t>(q * 32) << 16) + cb;
-#pragma unroll 1
+#pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t g[32], v[32];
             tmem_ld32(tb + c0, g);
             tmem_ld32(tb + BN / 2 + c0, v);
             tmem_ld_wait();
-            if (valid) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
-              for (int w4 = 0; w4 < 4; ++w4) {
-                uint32_t o[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const int c = 8 * w4 + 2 * i;
-                  o[i] = pack_bf16x2(silu_mul(__uint_as_float(g[c]), __uint_as_float(v[c])),
-                                     silu_mul(__uint_as_float(g[c + 1]), __uint_as_float(v[c + 1])));
-                }
-                dst[w4] = make_uint4(o[0], o[1], o[2], o[3]);
-              }
-            }
+            for (int i = 0; i < 16; ++i)
+              packed[c0 / 2 + i] =
+                  pack_bf16x2(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(v[2 * i])),
+                              silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(v[2 * i + 1])));
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->tempty[h]);
+        if (rows > 0) {
+          // lane l holds row q*32 + l: stage it, then store four whole rows per instruction
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t at = blk_s + lane * 128 + ((c ^ (lane & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(at), "r"(packed[4 * c]),
+                         "r"(packed[4 * c + 1]), "r"(packed[4 * c + 2]), "r"(packed[4 * c + 3])
+                         : "memory");
+          }
+          __syncwarp();
+          const int chunk = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3);  // row within this warp's 32
+            uint4 val;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                         : "r"(blk_s + rr * 128 + ((chunk ^ (rr & 7)) << 4))
+                         : "memory");
+            if (q * 32 + rr < rows)
+              *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(row0 + h * BM + q * 32 + rr) *
+                                                    p.ldo +
+                                        n0 + chunk * 8) = val;
+          }
+          __syncwarp();  // the staging block is read out before the next half reuses it
+        }
       }
     }
   }
