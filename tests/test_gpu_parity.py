@@ -277,9 +277,10 @@ def test_split_k_is_used_for_few_tiles_and_is_deterministic(oracle, make):
 
 def test_cta_pair_gemm2_with_odd_and_even_block_counts(oracle):
     """1500 tokens of the tiny layer (3000 assignments, at least two 128-row blocks per
-    expert on average) run GEMM 2 on CTA pairs over pairs of row blocks of one expert; a
-    bias makes one expert hot (many blocks) and others small (a lone last block, paired
-    with rows that are computed and not stored)."""
+    expert on average) run both GEMMs over the table of pairs of row blocks of one expert:
+    GEMM 1 as 256-row tiles on one SM, GEMM 2 on CTA pairs. A bias makes one expert hot
+    (many blocks) and others small, so some pairs hold a lone last block (GEMM 1 skips the
+    empty half; GEMM 2 computes rows that are not stored)."""
     shape = wl.TINY
     x = wl.make_x(17, 1500, shape.H)
     bias = np.array([3.0, 0.0, -1.0, 0.5, -2.0, 1.0, 0.0, -0.5])
