@@ -66,6 +66,9 @@ class Runner:
             "dev_err": R.rimuru_get_device_error(self.ev, clear=True),
         }
         r["tiles"] = self.region("tiles", torch.int32, 2 * r["num_tiles"]).cpu().numpy().reshape(-1, 2)
+        r["num_ptiles"] = int(self.region("num_ptiles", torch.int32, 1).cpu().item())
+        r["ptiles"] = (self.region("ptiles", torch.int32, 2 * r["num_ptiles"]).cpu().numpy()
+                       .reshape(-1, 2))
         return r
 
     def close(self):

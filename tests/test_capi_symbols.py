@@ -32,7 +32,17 @@ def test_status_strings():
     assert R.rimuru_status_string(0) == "RIMURU_OK"
     assert R.rimuru_status_string(-4) == "RIMURU_ERR_UNMAPPED"
     assert R.rimuru_kernel_name(R.K_GEMM1) == "moe_gemm1_swiglu"
+    assert R.rimuru_kernel_name(R.K_COUNT) is None
     assert R.rimuru_kernel_name(99) is None
+
+
+def test_kernel_slot_numbers_match_the_header():
+    """The binding's K_* constants are the header's RIMURU_K_* enumerators."""
+    from paged_moe_shared_gb300 import rimuru as R
+    text = open(os.path.join(ROOT, "include", "rimuru.h")).read()
+    slots = dict((m, int(v)) for m, v in re.findall(r"RIMURU_K_([A-Z0-9_]+)\s*=\s*(\d+)", text))
+    assert slots == {name: getattr(R, "K_" + name) for name in slots}
+    assert slots["COUNT"] == max(v for k, v in slots.items() if k != "COUNT") + 1
 
 
 def test_selftest_rejects_bad_limits_before_touching_a_device():

@@ -40,6 +40,11 @@ def check(res, w, o_res, tokens=None, hidden=True):
     assert res["num_tiles"] == blocks.sum()
     exp_tiles = [(e, o_res["offsets"][e] + 128 * b) for e in range(s.E) for b in range(blocks[e])]
     assert [tuple(t) for t in res["tiles"].tolist()] == exp_tiles
+    # pair table: each expert's blocks two by two (an odd last block alone), expert order
+    exp_pairs = [(e, o_res["offsets"][e] + 256 * b) for e in range(s.E)
+                 for b in range((blocks[e] + 1) // 2)]
+    assert res["num_ptiles"] == len(exp_pairs)
+    assert [tuple(t) for t in res["ptiles"].tolist()] == exp_pairs
     toks = np.arange(w.T) if tokens is None else np.asarray(tokens)
     err = rel_err(res["out"][toks], o_res["out"][toks])
     assert err <= TOL, f"out rel err {err:.3e}"
