@@ -181,26 +181,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           // A arrived through cp.async (generic proxy); the MMA reads it
           // through the async proxy
           fence_proxy_async_smem();
-          if (kb == 0 && has1) {
-            if (!mbar_wait(&sh->tempty[1], par, abort)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
           const uint32_t a0 = smem_u32(sA + s * kABytes);
           const uint32_t b0 = smem_u32(sB + s * kBBytes);
+          // A: K-major, 128-byte rows, 8-row groups 1024 B apart; +32 B per 16 k.
+          // B: MN-major, 64-column chunks kBChunk apart (LBO), 8-k-row groups
+          // 1024 B apart (SBO); +16 rows * 128 B per 16 k.
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; +32 B per 16 k.
-            // B: MN-major, 64-column chunks kBChunk apart (LBO), 8-k-row groups
-            // 1024 B apart (SBO); +16 rows * 128 B per 16 k.
-            const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kBChunk, 1024);
-            const uint32_t acc = (kb != 0 || kk != 0) ? 1u : 0u;
-            umma_bf16(tmem_base, smem_desc_sw128(a0 + kk * 32, 16, 1024), bd, idesc, acc);
-            if (has1)
-              umma_bf16(tmem_base + BN, smem_desc_sw128(a0 + kAHalfBytes + kk * 32, 16, 1024), bd,
-                        idesc, acc);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(tmem_base, smem_desc_sw128(a0 + kk * 32, 16, 1024),
+                      smem_desc_sw128(b0 + kk * 2048, kBChunk, 1024), idesc,
+                      (kb != 0 || kk != 0) ? 1u : 0u);
+          if (has1) {
+            // half 1 of the previous tile may still be draining: half 0's
+            // first MMAs are already queued while this thread waits for it
+            if (kb == 0) {
+              if (!mbar_wait(&sh->tempty[1], par, abort)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_bf16(tmem_base + BN, smem_desc_sw128(a0 + kAHalfBytes + kk * 32, 16, 1024),
+                        smem_desc_sw128(b0 + kk * 2048, kBChunk, 1024), idesc,
+                        (kb != 0 || kk != 0) ? 1u : 0u);
           }
           umma_commit(&sh->empty[s]);  // stage s is free once these MMAs are done
         }
