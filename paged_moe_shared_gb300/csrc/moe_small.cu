@@ -228,11 +228,14 @@ __device__ void write_tables(int E, int tot, int off, int32_t* __restrict__ offs
 // ----------------------------------------------------------------- align
 // One CTA per routing chunk (kChunkAssign threads).  Every CTA sums the chunk
 // histograms (all chunks -> totals, earlier chunks -> this chunk's base per
-// expert), with parts = blockDim / E threads per expert column; CTA 0 also
-// writes the offsets and the 128-row tile table.  Inside the chunk an
-// assignment's rank among same-expert assignments is the number of earlier
-// ones, which keeps the order stable.
-__global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
+// expert), with parts = blockDim / E threads per expert column, each issuing
+// its loads in batches; CTA 0 also writes the offsets and the tile tables.
+// Inside the chunk an assignment's rank among same-expert assignments is the
+// number of earlier ones: inside a warp by __match_any_sync, across warps by a
+// prefix over per-warp counts, which keeps the order stable.
+constexpr int kHistBatch = 8;  // chunk histogram loads in flight per thread
+
+__global__ void __launch_bounds__(kChunkAssign, 2) moe_align_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ chunk_hist, int chunks, int A,
     int E, int chunk, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted,
     int32_t* __restrict__ inv, int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles,
@@ -241,30 +244,57 @@ __global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
   __shared__ int s_part_tot[kChunkAssign];
   __shared__ int s_part_bef[kChunkAssign];
   __shared__ int s_base[kMaxExperts];
-  __shared__ int s_ids[kChunkAssign];
+  __shared__ uint16_t s_wh[kChunkAssign / 32][kMaxExperts];  // per-warp counts, then their prefix
   __shared__ int s_warp[32];
   grid_dep_wait();
   grid_dep_launch();
   const int c = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int f0 = c * chunk;
+  const int n = min(chunk, A - f0);
+  const int groups = (n + 31) / 32;
+  for (int i = tid; i < groups * E; i += blockDim.x) s_wh[i / E][i % E] = 0;
   const int parts = blockDim.x / E;  // >= 2 since E <= kMaxExperts = blockDim / 2
   {
     const int e = tid % E, part = tid / E;
     int tot = 0, bef = 0;
     if (part < parts) {
-      for (int cc = part; cc < chunks; cc += parts) {
-        const int n = chunk_hist[static_cast<size_t>(cc) * E + e];
-        tot += n;
-        if (cc < c) bef += n;
+      int cc = part;
+      for (; cc + (kHistBatch - 1) * parts < chunks; cc += kHistBatch * parts) {
+        int v[kHistBatch];
+#pragma unroll
+        for (int u = 0; u < kHistBatch; ++u)
+          v[u] = __ldg(chunk_hist + static_cast<size_t>(cc + u * parts) * E + e);
+#pragma unroll
+        for (int u = 0; u < kHistBatch; ++u) {
+          tot += v[u];
+          if (cc + u * parts < c) bef += v[u];
+        }
+      }
+      for (; cc < chunks; cc += parts) {
+        const int v = __ldg(chunk_hist + static_cast<size_t>(cc) * E + e);
+        tot += v;
+        if (cc < c) bef += v;
       }
     }
     s_part_tot[tid] = tot;
     s_part_bef[tid] = bef;
   }
-  const int f0 = c * chunk;
-  const int n = min(chunk, A - f0);
-  if (tid < n) s_ids[tid] = ids[f0 + tid];
-  __syncthreads();
+  // this thread's assignment f0 + tid: its expert and its rank in the warp
+  int my = -1, rank_in = 0, in_warp = 0;
+  const unsigned valid = __ballot_sync(kFull, tid < n);
+  if (tid < n) {
+    my = ids[f0 + tid];
+    if (my < 0 || my >= E) {
+      set_error(err, RIMURU_DEV_BAD_SHAPE);
+      my = -1;  // grouped apart, never scattered
+    }
+    const unsigned peers = __match_any_sync(valid, my);
+    rank_in = __popc(peers & ((1u << lane) - 1u));
+    in_warp = __popc(peers);
+  }
+  __syncthreads();  // s_wh zeroed, s_part_* written
+  if (my >= 0 && rank_in == 0) s_wh[warp][my] = static_cast<uint16_t>(in_warp);
   int tot = 0, before = 0;
   if (tid < E) {
     for (int p = 0; p < parts; ++p) {
@@ -272,23 +302,24 @@ __global__ void __launch_bounds__(kChunkAssign) moe_align_kernel(
       before += s_part_bef[p * E + tid];
     }
   }
-  const int off = block_exclusive_scan(tot, s_warp);
-  if (tid < E) s_base[tid] = off + before;
+  const int off = block_exclusive_scan(tot, s_warp);  // also orders the s_wh counts
+  if (tid < E) {
+    s_base[tid] = off + before;
+    int acc = 0;  // earlier warps' assignments of expert tid inside this chunk
+    for (int g = 0; g < groups; ++g) {
+      const int v = s_wh[g][tid];
+      s_wh[g][tid] = static_cast<uint16_t>(acc);
+      acc += v;
+    }
+  }
   if (c == 0)
     write_tables(E, tot, off, offsets, tiles, num_tiles, ptiles, num_ptiles, tile_cnt, cnt_len,
                  s_warp);
   __syncthreads();
-  if (tid < n) {
-    const int my = s_ids[tid];
-    if (my < 0 || my >= E) {
-      set_error(err, RIMURU_DEV_BAD_SHAPE);
-    } else {
-      int rank = 0;  // earlier assignments of the same expert inside this chunk
-      for (int j = 0; j < tid; ++j) rank += (s_ids[j] == my);
-      const int pos = s_base[my] + rank;
-      sorted[pos] = f0 + tid;
-      inv[f0 + tid] = pos;
-    }
+  if (my >= 0) {
+    const int pos = s_base[my] + s_wh[warp][my] + rank_in;
+    sorted[pos] = f0 + tid;
+    inv[f0 + tid] = pos;
   }
 }
 
