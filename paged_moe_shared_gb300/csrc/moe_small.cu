@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kChunkAssign) moe_route_align_gather_kernel(
 // out[t] = sum_j w[t*k+j] * y[inv[t*k+j]], j ascending, fp32, bf16 result.
 // Each thread owns one 16-byte column slice of a token and issues the loads of
 // up to eight slots before it accumulates them in slot order.
-__global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restrict__ y,
+__global__ void __launch_bounds__(256, 4) moe_combine_kernel(const uint4* __restrict__ y,
                                                           const int32_t* __restrict__ inv,
                                                           const float* __restrict__ w, int T,
                                                           int k, int H8, uint4* __restrict__ out) {
