@@ -52,3 +52,25 @@ def test_selftest_rejects_bad_limits_before_touching_a_device():
         with pytest.raises(R.RimuruError) as e:
             R.rimuru_selftest_bounded_wait(bad)
         assert e.value.status == R.ERR_ARG
+
+
+def header_struct_members(name):
+    """(type, member) pairs of `typedef struct <name> { ... } <name>;` in the header."""
+    text = open(os.path.join(ROOT, "include", "rimuru.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    body = re.search(r"typedef struct " + name + r"\s*\{(.*?)\}\s*" + name + r"\s*;", text, re.S)
+    assert body, name
+    return re.findall(r"\b(u?int(?:32|64)_t)\s+([a-z_0-9]+)\s*;", body.group(1))
+
+
+def test_binding_structs_match_the_header():
+    """The ctypes structures of the binding list the header's members in order, with the
+    same integer widths and signedness."""
+    import ctypes
+    from paged_moe_shared_gb300 import rimuru as R
+    ctype = {"uint64_t": ctypes.c_uint64, "int64_t": ctypes.c_int64, "int32_t": ctypes.c_int32,
+             "uint32_t": ctypes.c_uint32}
+    for cname, cls in (("rimuru_level_stats", R.LevelStats), ("rimuru_ws_layout", R.WsLayout),
+                       ("rimuru_offload_counters", R.OffloadCounters)):
+        members = header_struct_members(cname)
+        assert [(n, ctype[t]) for t, n in members] == list(cls._fields_), cname
