@@ -74,3 +74,45 @@ def test_binding_structs_match_the_header():
                        ("rimuru_offload_counters", R.OffloadCounters)):
         members = header_struct_members(cname)
         assert [(n, ctype[t]) for t, n in members] == list(cls._fields_), cname
+
+
+def header_prototypes():
+    """name -> (return type, [parameter types]) for every function the header declares."""
+    text = open(os.path.join(ROOT, "include", "rimuru.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    protos = {}
+    for ret, name, params in re.findall(r"([A-Za-z_][A-Za-z_0-9 ]*?\**)\s*\b(rimuru_[a-z0-9_]+)\s*\(([^)]*)\)\s*;",
+                                        text):
+        types = []
+        for p in params.split(","):
+            p = p.strip()
+            if p in ("", "void"):
+                continue
+            types.append(re.sub(r"\s*\b[a-z_0-9]+$", "", p) if not p.endswith("*") else p)
+        protos[name] = (ret.strip(), types)
+    return protos
+
+
+def test_binding_signatures_match_the_header():
+    """Every entry point's argument and result types in the binding agree with its C
+    prototype: pointers and handles as pointers, and integers of the same width and sign."""
+    import ctypes
+    from paged_moe_shared_gb300 import rimuru as R
+    ints = {"int": ctypes.c_int, "int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64,
+            "uint64_t": ctypes.c_uint64, "uint32_t": ctypes.c_uint32, "double": ctypes.c_double}
+
+    def agrees(ctype_str, ct):
+        c = ctype_str.replace("const ", "").strip()
+        if c.endswith("*") or c.endswith("_t") and c.startswith("rimuru_"):
+            return ct in (ctypes.c_void_p, ctypes.c_char_p) or hasattr(ct, "_type_") and \
+                issubclass(ct, ctypes._Pointer)
+        return ct is ints[c]
+
+    protos = header_prototypes()
+    assert len(protos) == len(R.EXPORTS)
+    for name, (ret, params) in protos.items():
+        fn = getattr(R.lib, name)
+        assert len(fn.argtypes) == len(params), (name, params, fn.argtypes)
+        for c, ct in zip(params, fn.argtypes):
+            assert agrees(c, ct), (name, c, ct)
+        assert agrees(ret, fn.restype), (name, ret, fn.restype)
