@@ -98,8 +98,10 @@ struct GemmArgs {
   int top_k;
   int ldx;
   // Weight prefetch before the grid dependency wait: the CTA guesses its first
-  // tile's expert as if every expert had prefetch_bpe row blocks and prefetches
-  // the first prefetch_kb k blocks of that tile's weights into L2 (0: off).
+  // tile's expert as if every expert had prefetch_bpe row blocks (0: reads it
+  // from the tile table, which must then come from a kernel that finished
+  // before the one this launch follows started) and prefetches the first
+  // prefetch_kb k blocks of that tile's weights into L2 (prefetch_kb 0: off).
   int prefetch_kb;
   int prefetch_bpe;
   int num_experts;

@@ -205,8 +205,14 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   // row block (at most half a block per expert on average); larger batches
   // reuse weights from L2, smaller ones would prefetch the wrong experts.
   if (A >= 2 * E && 2LL * A <= static_cast<long long>(E) * kTileM) {
-    g1.prefetch_kb = g2.prefetch_kb = kPrefetchKBlocks;
-    g1.prefetch_bpe = g2.prefetch_bpe = 1;
+    g1.prefetch_kb = kPrefetchKBlocks;
+    g1.prefetch_bpe = 1;
+  }
+  // GEMM 2 follows GEMM 1, which follows the kernel that wrote the tile table:
+  // it reads its first tile's expert from the table instead of guessing.
+  if (2LL * A <= static_cast<long long>(E) * kTileM) {
+    g2.prefetch_kb = kPrefetchKBlocks;
+    g2.prefetch_bpe = 0;
   }
   g1.num_experts = g2.num_experts = E;
 

@@ -113,7 +113,12 @@ __global__ void __launch_bounds__(kGatherA ? kThreadsGather : kThreads, 1)
     // while that kernel still runs.  A wrong guess costs bandwidth only.
     const int S = p.splits, nkb = p.num_k_blocks;
     const int tile = blockIdx.x / S, split = blockIdx.x - tile * S;
-    const int e = tile / p.n_blocks / p.prefetch_bpe, nb = tile % p.n_blocks;
+    const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
+    // prefetch_bpe = 0: the tile table was written by a kernel that finished
+    // before the one we follow started, so read it (at L2: no stale L1 line)
+    const int e = p.prefetch_bpe > 0 ? mb / p.prefetch_bpe
+                                     : (mb < __ldcg(p.num_tiles) ? __ldcg(p.tiles + 2 * mb)
+                                                                : p.num_experts);
     const int kb0 = split * nkb / S;
     const int kb1 = min(kb0 + p.prefetch_kb, (split + 1) * nkb / S);
     if (e < p.num_experts) {
