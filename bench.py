@@ -64,10 +64,13 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    """nvidia-smi sampling of SM clocks, throttle reasons and utilisation while the GPU legs
+    run.  A sample is under load when nvidia-smi saw a kernel executing in its period
+    (utilization.gpu > 0); the median SM clock is taken over those samples."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -94,26 +97,33 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.close()
-        mhz, maxmhz, reasons = [], 0.0, set()
+        mhz, loaded, maxmhz, reasons = [], [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    mhz.append(float(parts[1]))
+                    clk = float(parts[1])
                     maxmhz = max(maxmhz, float(parts[2]))
+                    util = float(parts[9])
                 except ValueError:
                     continue
+                mhz.append(clk)
+                if util > 0:
+                    loaded.append(clk)
                 for n, v in zip(names, parts[5:9]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
         os.remove(self.path)
         if not mhz:
             return None
-        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": maxmhz,
-                "reasons": sorted(reasons), "samples": len(mhz)}
+        return {"sm_mhz": statistics.median(loaded or mhz), "sm_max_mhz": maxmhz,
+                "reasons": sorted(reasons), "samples": len(mhz),
+                "samples_under_load": len(loaded),
+                "window": "every GPU leg of this run (timed region, bracketed pass, e2e, "
+                          "graph replays, prefill block)"}
 
 
 def source_digest(*rel_paths):
@@ -171,6 +181,14 @@ def kernel_work(w, counts):
                              "flops": 2 * A * H * 2 * I},
         "moe_gemm2": {"bytes": U * I * H * 2 + A * I * 2 + A * H * 2, "flops": 2 * A * I * H},
         "moe_combine": {"bytes": A * H * 2 + T * H * 2 + A * 8, "flops": 2 * A * H},
+        # decode path: decode_gemm1 streams W1/W3 into shared memory and prefetches the W2
+        # pages into L2 (it moves every weight byte of the layer from HBM), decode_gemm2
+        # reads W2 back from L2
+        "moe_decode_gemm1": {"bytes": U * 3 * H * I * 2 + T * E * 4 + T * H * 2,
+                             "flops": 2 * A * H * 2 * I},
+        "moe_decode_reduce": {"bytes": A * I * 2, "flops": 0},
+        "moe_decode_gemm2": {"bytes": U * I * H * 2 + A * I * 2 + T * H * 2,
+                             "flops": 2 * A * I * H + 2 * A * H},
         "layer": {"bytes": U * 3 * H * I * 2 + T * H * 2 + T * E * 4 + T * H * 2,
                   "flops": 6 * A * H * I},
         "U": U,
@@ -180,7 +198,9 @@ def kernel_work(w, counts):
 def run_offload(args, rank, world, local_rank):
     """48-layer offloaded stack: a step runs all layers once over T tokens; before layer l's
     forward every expert of layer l + 1 is prefetched (routing at 256 tokens touches nearly
-    all of them).  Bound by the host-to-device link, measured in the same run."""
+    all of them).  Bound by the host-to-device link, measured in the same run.  The line's
+    value uses least-recently-used eviction (the configuration's policy); the layer-cycle
+    policy is measured on the same stack and reported beside it."""
     import torch
 
     import workloads as wl
@@ -201,9 +221,6 @@ def run_offload(args, rank, world, local_rank):
     pool.mem.view(torch.int16).fill_(wl.BF16_NAN)
     ev = pool.view(pb)
     R.rimuru_view_set_moe_shape(ev, L, E, H, I, shape.k, shape.renorm)
-    off = R.rimuru_offload_create(ev, host.data_ptr(), cap, 0)
-    policy = R.EVICT_LAYER_CYCLE if args.evict == "layer_cycle" else R.EVICT_LRU
-    R.rimuru_offload_set_policy(off, policy)
     xs = [torch.from_numpy(st.x_bits[0][i].view(np.int16)).view(torch.bfloat16).to(dev)
           for i in range(8)]
     lgs = [torch.from_numpy(st.logits[0][i]).to(dev) for i in range(8)]
@@ -213,37 +230,47 @@ def run_offload(args, rank, world, local_rank):
     ws_ptr = (ws_raw.data_ptr() + 1023) // 1024 * 1024
     stream = torch.cuda.current_stream()
     all_experts = list(range(E))
-
-    def one_step(step):
-        for l in range(L):
-            R.rimuru_offload_prefetch(off, (l + 1) % L, all_experts)
-            i = (step * L + l) % 8
-            R.rimuru_offload_forward(off, xs[i].data_ptr(), lgs[i].data_ptr(), T, l, out.data_ptr(),
-                                     ws_ptr, ws_bytes, stream.cuda_stream)
-
-    for w in range(args.warmup):
-        one_step(w)
-    torch.cuda.synchronize()
-    c0 = R.rimuru_offload_stats(off)
     K = args.steps
     clocks = ClockSampler(local_rank)
     clocks.start()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k_ in range(K):
-        one_step(args.warmup + k_)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
+
+    def run_policy(policy):
+        off = R.rimuru_offload_create(ev, host.data_ptr(), cap, 0)
+        R.rimuru_offload_set_policy(off, policy)
+
+        def one_step(step):
+            for l in range(L):
+                R.rimuru_offload_prefetch(off, (l + 1) % L, all_experts)
+                i = (step * L + l) % 8
+                R.rimuru_offload_forward(off, xs[i].data_ptr(), lgs[i].data_ptr(), T, l,
+                                         out.data_ptr(), ws_ptr, ws_bytes, stream.cuda_stream)
+
+        try:
+            for w in range(args.warmup):
+                one_step(w)
+            torch.cuda.synchronize()
+            c0 = R.rimuru_offload_stats(off)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k_ in range(K):
+                one_step(args.warmup + k_)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - t0
+            ms = e0.elapsed_time(e1)
+            c1 = R.rimuru_offload_stats(off)
+            if R.rimuru_get_device_error(ev) != R.DEV_OK:
+                raise RuntimeError("device error in the timed region")
+        finally:
+            R.rimuru_offload_destroy(off)
+        return ms, {k: c1[k] - c0[k] for k in c1}, wall
+
+    ms_lru, d_lru, wall_lru = run_policy(R.EVICT_LRU)
+    ms_cyc, d_cyc, wall_cyc = run_policy(R.EVICT_LAYER_CYCLE)
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    c1 = R.rimuru_offload_stats(off)
-    if R.rimuru_get_device_error(ev) != R.DEV_OK:
-        raise RuntimeError("device error in the timed region")
-    d = {k: c1[k] - c0[k] for k in c1}
-    # the link, measured the same way the cache uses it: pinned host -> device, large copies
+    # the link, measured the way the cache uses it: pinned host -> device, large copies
     src = host[: 1 << 30]
     dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
     for _ in range(2):
@@ -255,23 +282,32 @@ def run_offload(args, rank, world, local_rank):
     b1.record(stream)
     torch.cuda.synchronize()
     link_gbs = 5 * (1 << 30) / (b0.elapsed_time(b1) / 1e3) / 1e9
-    achieved = d["bytes_h2d"] / (ms / 1e3) / 1e9
-    R.rimuru_offload_destroy(off)
     pool.close()
+
+    def roof(d, ms):
+        a = d["bytes_h2d"] / (ms / 1e3) / 1e9
+        return {"bound": "h2d", "achieved": round(a, 1), "peak": round(link_gbs, 1),
+                "unit": "GB/s", "frac": round(a / link_gbs, 4), "traffic": None,
+                "peak_source": "pinned host->device copy measured in this run"}
+
     return {
         "metric": "offloaded 48-layer paged MoE stack tokens/s (Qwen3-30B-A3B layers)",
-        "value": round(T * K / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(ms / K, 3), "higher_is_better": True,
+        "value": round(T * K / (ms_lru / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_lru / K, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"q3_stack_offload: {WORKLOAD_TEXT['q3_stack_offload']}",
-                   "layers": L, "tokens": T, "resident_experts": cap, "eviction": args.evict,
+                   "layers": L, "tokens": T, "resident_experts": cap, "eviction": "lru",
                    "host_pages_gib": round(host.numel() / 2**30, 1),
                    "l2": "inputs larger than L2 (the stack reads 54 GiB of expert pages)"},
-        "roofline": {"bound": "h2d", "achieved": round(achieved, 1), "peak": round(link_gbs, 1),
-                     "unit": "GB/s", "frac": round(achieved / link_gbs, 4), "traffic": None,
-                     "peak_source": "pinned host->device copy measured in this run"},
-        "cache": {k: int(v) for k, v in d.items()},
-        "wall_s": round(wall, 3), "clocks": clk,
+        "roofline": roof(d_lru, ms_lru),
+        "cache": {k: int(v) for k, v in d_lru.items()},
+        "wall_s": round(wall_lru, 3),
+        "layer_cycle": {"value": round(T * K / (ms_cyc / 1e3), 1), "unit": "tokens/s",
+                        "ms_per_step": round(ms_cyc / K, 3), "eviction": "layer_cycle",
+                        "roofline": roof(d_cyc, ms_cyc),
+                        "cache": {k: int(v) for k, v in d_cyc.items()},
+                        "wall_s": round(wall_cyc, 3)},
+        "clocks": clk,
         "gpu_launches": len(LAYER_KERNELS) * L * K,
     }
 
@@ -299,101 +335,156 @@ def layers_to_cycle(w) -> int:
     return int(min(256, -(-3 * L2_BYTES // step_bytes)))
 
 
-def run_ours(args, rank, world, local_rank):
+def workload_config(w, args_workload, seed, U, n_layers, layer_bytes, world):
+    """The `config` object of a line: the same dict from both arms for the same workload."""
+    return {"workload": f"{args_workload}: {WORKLOAD_TEXT[args_workload]}", "tokens": w.T,
+            "experts_touched": int(U), "seed": seed,
+            "l2": "inputs larger than L2: the expert pages read per step exceed 129 MB"
+            if n_layers == 1 else
+            f"a layer's pages fit in L2, so steps cycle over {n_layers} copies of the "
+            f"layer (same weights, distinct pool pages): "
+            f"{n_layers * layer_bytes / 1e6:.0f} MB per cycle",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def roofline_of(work, kernel, ms, peaks, bound):
+    """Algorithmic work of one launch over its mean CUDA-event duration, against the
+    measured peak: HBM copy GB/s, or bf16 TFLOP/s both as a burst (a kernel timed on its
+    own, short loop: this one governs here) and sustained (a seconds-long loop)."""
+    t = ms / 1e3
+    if bound == "hbm":
+        a = work[kernel]["bytes"] / t / 1e9
+        return {"bound": "hbm", "achieved": round(a, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(a / peaks["hbm_gbs"], 4),
+                "peak_source": peaks["source"] + " (HBM copy)"}
+    a = work[kernel]["flops"] / t / 1e12
+    return {"bound": "tensor", "achieved": round(a, 1), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(a / peaks["bf16_tflops"], 4),
+            "peak_sustained": peaks["bf16_tflops_sustained"],
+            "frac_of_sustained": round(a / peaks["bf16_tflops_sustained"], 4),
+            "peak_source": peaks["source"] + " (bf16 burst; the loop timed here is short)"}
+
+
+class Layer:
+    """A workload placed in a device pool, with its inputs, output and workspace."""
+
+    def __init__(self, w, dev, n_layers=1, pool=None, ev=None, decode_tokens=None):
+        import torch
+
+        from paged_moe_shared_gb300 import rimuru as R
+        from paged_moe_shared_gb300.device_pool import load_workload, replicate_layers
+        self.R = R
+        self.w = w
+        self.dev = dev
+        self.n_layers = n_layers
+        self.own_pool = pool is None
+        if pool is None:
+            extra = (n_layers - 1) * 3 * w.shape.E
+            pool, ev, _ = load_workload(w, dev, layers=n_layers, extra_pages=extra)
+            replicate_layers(pool, ev, w, n_layers)
+        self.pool, self.ev = pool, ev
+        if decode_tokens is not None:
+            R.rimuru_view_set_decode_tokens(ev, decode_tokens)
+        self.counter = 0
+        self.x = torch.from_numpy(w.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.logits = torch.from_numpy(w.logits).to(dev)
+        self.out = torch.empty_like(self.x)
+        self.ws_bytes = R.rimuru_moe_workspace_bytes(ev, w.T)
+        self.ws_raw = torch.empty(self.ws_bytes + 1024, dtype=torch.uint8, device=dev)
+        self.ws_ptr = (self.ws_raw.data_ptr() + 1023) // 1024 * 1024
+        self.stream = torch.cuda.current_stream()
+
+    def step(self, on=None):
+        layer = self.counter % self.n_layers
+        self.counter += 1
+        self.R.rimuru_moe_forward(self.x.data_ptr(), self.logits.data_ptr(), self.w.T, self.ev,
+                                  layer, self.out.data_ptr(), self.ws_ptr, self.ws_bytes,
+                                  (on or self.stream).cuda_stream)
+
+    def counts(self):
+        import torch
+        lay = self.R.rimuru_moe_workspace_layout(self.ev, self.w.T)
+        at = self.ws_ptr - self.ws_raw.data_ptr() + lay["offsets"]
+        offs = self.ws_raw[at:at + (self.w.shape.E + 1) * 4].view(torch.int32).cpu().numpy()
+        return np.diff(offs)
+
+    def close(self):
+        if self.own_pool:
+            self.pool.close()
+
+
+def measure(L, args, K, world, dist, dev, full=True):
+    """Time K forwards of one layer (after args.warmup untimed ones): `value`, the per-kernel
+    table, the dominant kernel in a bracketed pass, and (full) e2e and CUDA-graph legs."""
     import torch
-
-    import workloads as wl
-    from paged_moe_shared_gb300 import rimuru as R
-    from paged_moe_shared_gb300.device_pool import load_workload, replicate_layers
-
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    torch.cuda.set_device(local_rank)
-    dev = f"cuda:{local_rank}"
-    w = make_workload(args)
-    # A layer whose expert pages fit in L2 would be re-read from L2 on every step; such
-    # workloads cycle over identical copies of the layer at different pool addresses.
-    n_layers = layers_to_cycle(w)
-    extra = (n_layers - 1) * 3 * w.shape.E
-    pool, ev, _ = load_workload(w, dev, layers=n_layers, extra_pages=extra)
-    replicate_layers(pool, ev, w, n_layers)
-    counter = [0]
-    x = torch.from_numpy(w.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
-    logits = torch.from_numpy(w.logits).to(dev)
-    out = torch.empty_like(x)
-    ws_bytes = R.rimuru_moe_workspace_bytes(ev, w.T)
-    ws_raw = torch.empty(ws_bytes + 1024, dtype=torch.uint8, device=dev)
-    ws_ptr = (ws_raw.data_ptr() + 1023) // 1024 * 1024
-    stream = torch.cuda.current_stream()
-
-    def step(on=None):
-        layer = counter[0] % n_layers
-        counter[0] += 1
-        R.rimuru_moe_forward(x.data_ptr(), logits.data_ptr(), w.T, ev, layer, out.data_ptr(),
-                             ws_ptr, ws_bytes, (on or stream).cuda_stream)
+    R = L.R
+    w = L.w
 
     def barrier():
         if dist is not None:
             dist.barrier()
 
     for _ in range(args.warmup):
-        step()
+        L.step()
     torch.cuda.synchronize()
-    if R.rimuru_get_device_error(ev) != R.DEV_OK:
+    if R.rimuru_get_device_error(L.ev) != R.DEV_OK:
         raise RuntimeError("device error during warm-up")
-    lay = R.rimuru_moe_workspace_layout(ev, w.T)
-    at = ws_ptr - ws_raw.data_ptr() + lay["offsets"]
-    offs = ws_raw[at:at + (w.shape.E + 1) * 4].view(torch.int32).cpu().numpy()
-    counts = np.diff(offs)
-    work = kernel_work(w, counts)
+    work = kernel_work(w, L.counts())
 
     # -------------------------------------------- per-kernel table (untimed, all kernels)
     # Event pairs between kernels stop each kernel from overlapping its predecessor, so this
-    # pass is separate from the timed region and only picks the dominant kernel.
-    Kp = min(args.steps, 200)
-    R.rimuru_profile_enable(ev, R.PROFILE_ALL, Kp)
+    # pass is separate from the timed region; it gives every kernel's share.
+    Kp = min(K, 200)
+    R.rimuru_profile_enable(L.ev, R.PROFILE_ALL, Kp)
     for _ in range(Kp):
-        step()
+        L.step()
     torch.cuda.synchronize()
-    R.rimuru_profile_enable(ev, 0, 1)
+    R.rimuru_profile_enable(L.ev, 0, 1)
     per_kernel = {}
     for kidx in range(R.K_COUNT):
-        n, ms = R.rimuru_profile_read(ev, kidx)
+        n, ms = R.rimuru_profile_read(L.ev, kidx)
         if n:  # kernels the layer's path does not launch report no launches
             per_kernel[R.rimuru_kernel_name(kidx)] = {"launches": n, "ms_per_launch": ms / n}
     launches_per_step = sum(v["launches"] for v in per_kernel.values()) // Kp
-    dom = max(("moe_gemm1_swiglu", "moe_gemm2"), key=lambda n: per_kernel[n]["ms_per_launch"])
-    dom_idx = [R.rimuru_kernel_name(i) for i in range(R.K_COUNT)].index(dom)
+    gemms = [n for n in ("moe_gemm1_swiglu", "moe_gemm2", "moe_decode_gemm1", "moe_decode_gemm2")
+             if n in per_kernel]
+    dom = max(gemms, key=lambda n: per_kernel[n]["ms_per_launch"])
+    names = [R.rimuru_kernel_name(i) for i in range(R.K_COUNT)]
+    dom_idx = names.index(dom)
 
     # ---------------------------------------------------------------- timed region
-    # The dominant kernel is bracketed by events (for the roofline) in one forward out of
-    # PROFILE_EVERY: an event pair keeps the kernel from overlapping its neighbours, so
-    # bracketing every forward would slow the measured step.
-    K = args.steps
-    R.rimuru_profile_enable_sampled(ev, 1 << dom_idx, -(-K // PROFILE_EVERY), PROFILE_EVERY)
-    clocks = ClockSampler(local_rank)
-    clocks.start()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    t0.record(stream)
+    t0.record(L.stream)
     for _ in range(K):
-        step()
-    t1.record(stream)
+        L.step()
+    t1.record(L.stream)
     torch.cuda.synchronize()
     barrier()
-    clk = clocks.stop()
-    ms_total = t0.elapsed_time(t1)
-    R.rimuru_profile_enable(ev, 0, 1)
-    n_dom, ms_dom = R.rimuru_profile_read(ev, dom_idx)
-    dom_ms_live = ms_dom / max(n_dom, 1)
-    if R.rimuru_get_device_error(ev) != R.DEV_OK:
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
+    if R.rimuru_get_device_error(L.ev) != R.DEV_OK:
         raise RuntimeError("device error in the timed region")
-    ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / K
-    value = world * w.T * K / (ms_total / 1e3)
+
+    # ------------------------------------------- dominant kernel, bracketed pass
+    # Right after the timed region, the same forwards with the dominant kernel bracketed by
+    # an event pair on the launching stream in every one of them (a pair keeps that kernel
+    # from overlapping its neighbours, so the timed region above is left unbracketed).
+    Kb = max(K, 10)
+    R.rimuru_profile_enable(L.ev, 1 << dom_idx, Kb)
+    for _ in range(Kb):
+        L.step()
+    torch.cuda.synchronize()
+    n_dom, ms_dom = R.rimuru_profile_read(L.ev, dom_idx)
+    R.rimuru_profile_enable(L.ev, 0, 1)
+    dom_ms = ms_dom / max(n_dom, 1)
+
+    res = {"value": world * w.T * K / (ms_total / 1e3), "ms_per_step": ms_step, "work": work,
+           "per_kernel": per_kernel, "dom": dom, "dom_ms": dom_ms, "n_dom": n_dom,
+           "launches_per_step": launches_per_step, "Kp": Kp}
+    if not full:
+        return res
 
     # ---------------------------------------------------------------- end to end
     # Through rimuru_moe_forward_host: each step copies its x and logits in from pinned host
@@ -402,7 +493,7 @@ def run_ours(args, rank, world, local_rank):
     # buffering, as a serving loop would), so one step's copies overlap the other's kernels;
     # the single-stream figure is reported beside it.
     Ke = min(K, args.e2e_steps)
-    hws = R.rimuru_moe_host_workspace_bytes(ev, w.T)
+    hws = R.rimuru_moe_host_workspace_bytes(L.ev, w.T)
     lanes = []
     for _ in range(2):
         raw = torch.empty(hws + 1024, dtype=torch.uint8, device=dev)
@@ -411,12 +502,12 @@ def run_ours(args, rank, world, local_rank):
             "ws": (raw.data_ptr() + 1023) // 1024 * 1024,
             "x": torch.from_numpy(w.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory(),
             "logits": torch.from_numpy(w.logits).pin_memory(),
-            "out": torch.empty(tuple(x.shape), dtype=torch.bfloat16).pin_memory()})
+            "out": torch.empty(tuple(L.x.shape), dtype=torch.bfloat16).pin_memory()})
 
     def host_step(lane):
-        layer = counter[0] % n_layers
-        counter[0] += 1
-        R.rimuru_moe_forward_host(lane["x"].data_ptr(), lane["logits"].data_ptr(), w.T, ev,
+        layer = L.counter % L.n_layers
+        L.counter += 1
+        R.rimuru_moe_forward_host(lane["x"].data_ptr(), lane["logits"].data_ptr(), w.T, L.ev,
                                   layer, lane["out"].data_ptr(), lane["ws"], hws,
                                   lane["stream"].cuda_stream)
 
@@ -426,39 +517,45 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e0.record(L.stream)
         for ln in lanes[:n_lanes]:
             ln["stream"].wait_event(e0)
         for i in range(Ke):
             host_step(lanes[i % n_lanes])
         for ln in lanes[:n_lanes]:
-            stream.wait_stream(ln["stream"])
-        e1.record(stream)
+            L.stream.wait_stream(ln["stream"])
+        e1.record(L.stream)
         torch.cuda.synchronize()
         barrier()
         return max_over_ranks(e0.elapsed_time(e1), dist, dev)
 
     ms_e2e_serial = timed_host_steps(1)
     ms_e2e = timed_host_steps(2)
-    if R.rimuru_get_device_error(ev) != R.DEV_OK:
+    if R.rimuru_get_device_error(L.ev) != R.DEV_OK:
         raise RuntimeError("device error in the end-to-end steps")
-    ref_out = out.cpu()
+    ref_out = L.out.cpu()
     for ln in lanes:  # same inputs, deterministic layer: the host results equal the device's
         if not torch.equal(ln["out"].view(torch.int16), ref_out.view(torch.int16)):
             raise RuntimeError("host-buffer forward disagrees with the device-buffer forward")
-    e2e_value = world * w.T * Ke / (ms_e2e / 1e3)
+    res["e2e"] = {"value": round(world * w.T * Ke / (ms_e2e / 1e3), 1), "unit": "tokens/s",
+                  "h2d_bytes_per_step": int(L.x.numel() * 2 + L.logits.numel() * 4),
+                  "d2h_bytes_per_step": int(L.out.numel() * 2), "steps": Ke,
+                  "ms_per_step": round(ms_e2e / Ke, 5),
+                  "api": "rimuru_moe_forward_host (pinned host buffers)", "streams": 2,
+                  "single_stream_value": round(world * w.T * Ke / (ms_e2e_serial / 1e3), 1)}
+    del lanes
 
     # ------------------------------------------------------------ CUDA-graph replay
     # The same device-resident forwards recorded once by stream capture and replayed, as a
     # decode loop with fixed buffers would run them (reported beside `value`, which
     # launches every forward from the host).
-    G = max(n_layers, 10)
+    G = max(L.n_layers, 10)
     gs = torch.cuda.Stream(dev)
-    gs.wait_stream(stream)
+    gs.wait_stream(L.stream)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=gs):
         for _ in range(G):
-            step(gs)
+            L.step(gs)
     reps = max(1, K // G)
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(gs):  # replay() launches on the current stream
@@ -473,79 +570,126 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     ms_graph = max_over_ranks(g0.elapsed_time(g1), dist, dev)
-    if R.rimuru_get_device_error(ev) != R.DEV_OK:
+    if R.rimuru_get_device_error(L.ev) != R.DEV_OK:
         raise RuntimeError("device error in the graph replays")
-    graph_value = world * w.T * reps * G / (ms_graph / 1e3)
+    res["cuda_graph"] = {"value": round(world * w.T * reps * G / (ms_graph / 1e3), 1),
+                         "unit": "tokens/s", "ms_per_step": round(ms_graph / (reps * G), 5),
+                         "forwards_per_graph": G, "replays": reps}
     del graph
+    return res
 
-    # ---------------------------------------------------------------- roofline
-    peaks = load_peaks()
-    # the binding roofline of the dominant kernel: whichever of its byte time and its
-    # flop time at the measured peaks is longer
-    decode_like = (work[dom]["bytes"] / (peaks["hbm_gbs"] * 1e9)
-                   >= work[dom]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12))
-    t_dom = dom_ms_live / 1e3
-    if decode_like:
-        achieved = work[dom]["bytes"] / t_dom / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    else:
-        achieved = work[dom]["flops"] / t_dom / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1),
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops_sustained"], 4)}
-    roof["kernel"] = dom
-    roof["ms_per_launch"] = round(dom_ms_live, 5)
-    roof["launches_timed"] = n_dom
-    roof["timed_one_launch_in"] = PROFILE_EVERY
-    roof["traffic"] = ncu_traffic(dom, args.workload)
-    roof["peak_source"] = peaks["source"] + (" (sustained bf16)" if not decode_like else " (HBM copy)")
+
+def summarise(m, peaks, bound=None):
+    """roofline (dominant kernel), layer_roofline and the per-kernel table of a measurement."""
+    work, dom = m["work"], m["dom"]
+    if bound is None:  # whichever of the kernel's byte time and flop time is longer
+        bound = ("hbm" if work[dom]["bytes"] / (peaks["hbm_gbs"] * 1e9)
+                 >= work[dom]["flops"] / (peaks["bf16_tflops"] * 1e12) else "tensor")
+    roof = roofline_of(work, dom, m["dom_ms"], peaks, bound)
+    roof.update({"kernel": dom, "ms_per_launch": round(m["dom_ms"], 5),
+                 "launches_timed": m["n_dom"],
+                 "timing": "CUDA events on the launching stream around every launch of this "
+                           "kernel in a pass of forwards right after the timed region"})
+    per_kernel = m["per_kernel"]
     total_k = sum(v["ms_per_launch"] for v in per_kernel.values())
+    table = {}
     for name, v in per_kernel.items():
-        v["share"] = round(v["ms_per_launch"] / total_k, 4) if total_k else None
         tk = v["ms_per_launch"] / 1e3
+        row = {"launches": v["launches"], "ms_per_launch": round(v["ms_per_launch"], 5),
+               "share": round(v["ms_per_launch"] / total_k, 4) if total_k else None}
         if tk > 0:
-            v["GB/s"] = round(work[name]["bytes"] / tk / 1e9, 1)
+            row["GB/s"] = round(work[name]["bytes"] / tk / 1e9, 1)
             if work[name]["flops"]:
-                v["TFLOP/s"] = round(work[name]["flops"] / tk / 1e12, 1)
-        v["ms_per_launch"] = round(v["ms_per_launch"], 5)
-    layer_t = ms_step / 1e3
-    layer_roof = {"hbm_frac": round(work["layer"]["bytes"] / layer_t / 1e9 / peaks["hbm_gbs"], 4),
-                  "tensor_frac": round(work["layer"]["flops"] / layer_t / 1e12
-                                       / peaks["bf16_tflops_sustained"], 4)}
+                row["TFLOP/s"] = round(work[name]["flops"] / tk / 1e12, 1)
+        table[name] = row
+    lt = m["ms_per_step"] / 1e3
+    layer = {"hbm_frac": round(work["layer"]["bytes"] / lt / 1e9 / peaks["hbm_gbs"], 4),
+             "tensor_frac": round(work["layer"]["flops"] / lt / 1e12 / peaks["bf16_tflops"], 4),
+             "tensor_frac_of_sustained": round(work["layer"]["flops"] / lt / 1e12
+                                               / peaks["bf16_tflops_sustained"], 4)}
+    return roof, layer, table
 
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import workloads as wl
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    peaks = load_peaks()
+    w = make_workload(args)
+    # A layer whose expert pages fit in L2 would be re-read from L2 on every step; such
+    # workloads cycle over identical copies of the layer at different pool addresses.
+    n_layers = layers_to_cycle(w)
+    L = Layer(w, dev, n_layers, decode_tokens=args.decode_tokens)
+    clocks = ClockSampler(local_rank)  # from here on the run is GPU work (and host launches)
+    clocks.start()
+    K = args.steps
+    m = measure(L, args, K, world, dist, dev)
+    roof, layer_roof, table = summarise(m, peaks)
+    roof["traffic"] = ncu_traffic(m["dom"], args.workload)
+    work = m["work"]
     result = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "metric": METRIC, "value": round(m["value"], 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(m["ms_per_step"], 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}", "tokens": w.T,
-                   "experts_touched": work["U"], "seed": args.seed,
-                   "l2": "inputs larger than L2: the expert pages read per step exceed 129 MB"
-                   if n_layers == 1 else
-                   f"a layer's pages fit in L2, so steps cycle over {n_layers} copies of the "
-                   f"layer (same weights, distinct pool pages): "
-                   f"{n_layers * work['layer']['bytes'] / 1e6:.0f} MB per cycle",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": workload_config(w, args.workload, args.seed, work["U"], n_layers,
+                                  work["layer"]["bytes"], world),
         "roofline": roof,
         "layer_roofline": layer_roof,
-        "kernels": per_kernel,
-        "kernels_note": f"per-kernel event pairs around every launch, {Kp} untimed steps",
-        "gpu_launches": launches_per_step * K,
-        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(x.numel() * 2 + logits.numel() * 4),
-                "d2h_bytes_per_step": int(out.numel() * 2), "steps": Ke,
-                "ms_per_step": round(ms_e2e / Ke, 5),
-                "api": "rimuru_moe_forward_host (pinned host buffers)", "streams": 2,
-                "single_stream_value": round(world * w.T * Ke / (ms_e2e_serial / 1e3), 1)},
-        "cuda_graph": {"value": round(graph_value, 1), "unit": "tokens/s",
-                       "ms_per_step": round(ms_graph / (reps * G), 5),
-                       "forwards_per_graph": G, "replays": reps},
-        "clocks": clk,
+        "kernels": table,
+        "kernels_note": f"per-kernel event pairs around every launch, {m['Kp']} untimed steps",
+        "gpu_launches": m["launches_per_step"] * K,
+        "e2e": m["e2e"],
+        "cuda_graph": m["cuda_graph"],
     }
+
+    # ------------------------------------------------------------ prefill block
+    # The Qwen3-30B-A3B-shaped decode layer's pool is also the prefill layer's (same seed and
+    # pool size give the same weights and placement), so the default run measures the
+    # 8192-token Zipf prefill on the same pool, against the bf16 tensor peak.
+    if args.workload == "q3_decode" and not args.no_prefill and args.tokens is None \
+            and args.pool_pages is None:
+        pre = {}
+        for gamma in (0.5, 2.0):
+            x, lg = wl.q3_prefill_inputs(args.seed, 8192, gamma)
+            wp = wl.with_inputs(w, "q3_prefill_zipf", 8192, x, lg, {"zipf_gamma": gamma})
+            Lp = Layer(wp, dev, 1, pool=L.pool, ev=L.ev)
+            mp = measure(Lp, args, K, world, dist, dev, full=(gamma == 0.5))
+            proof, player, ptable = summarise(mp, peaks, bound="tensor")
+            c = Lp.counts()
+            entry = {"value": round(mp["value"], 1), "unit": "tokens/s",
+                     "ms_per_step": round(mp["ms_per_step"], 5), "steps": K,
+                     "config": {**workload_config(wp, "q3_prefill_zipf", args.seed,
+                                                  mp["work"]["U"], 1,
+                                                  mp["work"]["layer"]["bytes"], world),
+                                "zipf_gamma": gamma, "experts_empty": int((c == 0).sum()),
+                                "assignments_per_expert": [int(c.min()), int(c.max())]},
+                     "layer_roofline": player, "gpu_launches": mp["launches_per_step"] * K}
+            if gamma == 0.5:
+                proof["traffic"] = ncu_traffic(mp["dom"], "q3_prefill_zipf")
+                entry.update({"roofline": proof, "kernels": ptable, "e2e": mp["e2e"],
+                              "cuda_graph": mp["cuda_graph"]})
+                if rank == 0 and not args.no_cpu_baseline:
+                    entry["cpu_baseline"] = cpu_baseline(wp, args.cpu_seconds / 2)
+                pre["gamma_0.5"] = entry
+            else:
+                entry["roofline"] = {k: proof[k] for k in ("kernel", "achieved", "frac",
+                                                           "frac_of_sustained", "unit")}
+                pre["gamma_2"] = entry
+            Lp.close()
+        result["prefill"] = {**pre["gamma_0.5"], "heavy_skew": pre["gamma_2"]}
+
+    result["clocks"] = clocks.stop()
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
-    pool.close()
+    L.close()
     if dist is not None:
         dist.destroy_process_group()
     return result
@@ -585,8 +729,14 @@ def cpu_baseline(w, budget_s):
 
 
 def run_reference(args):
-    import workloads as wl
+    import oracle
     w = make_workload(args)
+    # the same config object as the GPU arm: routing (for the experts touched) and the L2 rule
+    o = oracle.Oracle()
+    ids, _ = o.route(w.logits, w.shape.k, w.shape.renorm)
+    counts = np.bincount(ids.ravel(), minlength=w.shape.E)
+    U = int((counts > 0).sum())
+    n_layers = layers_to_cycle(w)
     # every step is a sample of the workload's tokens, sized so that warm-up plus timed
     # steps take about REF_SECONDS on the host cores (one token per step at the least)
     per_step = REF_SECONDS / max(args.steps + args.warmup, 1)
@@ -607,8 +757,9 @@ def run_reference(args):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}", "tokens": w.T,
-                   "parallelism": "host cores"},
+        "config": workload_config(w, args.workload, args.seed, U, n_layers,
+                                  kernel_work(w, counts)["layer"]["bytes"], 1),
+        "where": "host cores",
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
                          "kind": "oracle",
                          "sample": f"{n} of {w.T} tokens per step (routing for all {w.T})"},
@@ -631,10 +782,12 @@ def main():
                     help="scale of the Zipf logit bias (q3_prefill_zipf; default 0.5)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=500)
-    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--cpu-seconds", type=float, default=16.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--evict", default="layer_cycle", choices=["layer_cycle", "lru"],
-                    help="eviction policy of the offload cache (q3_stack_offload)")
+    ap.add_argument("--decode-tokens", type=int, default=None,
+                    help="largest batch that takes the decode path (library default 4; 0: off)")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="q3_decode: skip the 8192-token prefill block of the default line")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = REF_DEFAULT_STEPS if args.impl == "reference" else DEFAULT_STEPS[args.workload]

@@ -75,3 +75,38 @@ def test_bf16_bits_round_to_nearest_even():
     # 1 + 3 * 2^-8 is halfway between 1 + 2^-7 and 1 + 2^-6: the even one is 1 + 2^-6
     np.testing.assert_array_equal(wl.bf16_bits_to_f32(bits),
                                   np.array([1.0, 1.0, 1.0 + 2 ** -6, -2.5, 65536.0], np.float32))
+
+
+def test_prefill_inputs_reuse_the_decode_pool():
+    """The bench measures prefill on the decode layer's pool: at the same seed and pool size
+    the prefill workload has the same pool bytes and page table, and q3_prefill_inputs gives
+    its x and logits."""
+    a = wl.q3_prefill_zipf(3, T=96, pool_pages=400)
+    b = wl.q3_decode(3, T=8, pool_pages=400)
+    x, lg = wl.q3_prefill_inputs(3, T=96)
+    assert np.array_equal(a.pool, b.pool) and np.array_equal(a.page_table, b.page_table)
+    assert np.array_equal(a.x_bits, x) and np.array_equal(a.logits, lg)
+    c = wl.with_inputs(b, "q3_prefill_zipf", 96, x, lg)
+    assert c.pool is b.pool and c.T == 96 and c.A == 96 * 8
+
+
+def test_covering_sample_reaches_every_block():
+    """covering_tokens picks tokens whose assignment rows include each expert's first and
+    last row and one row of each of its 128-row blocks (random skewed routing, stable
+    grouping by numpy)."""
+    from gpu_harness import covering_tokens
+    rng = np.random.default_rng(5)
+    T, k, E = 3000, 4, 16
+    p = 1.0 / np.arange(1, E + 1) ** 1.5
+    ids = np.stack([rng.choice(E, k, replace=False, p=p / p.sum()) for _ in range(T)])
+    srt = np.argsort(ids.ravel(), kind="stable").astype(np.int32)
+    offs = np.concatenate([[0], np.cumsum(np.bincount(ids.ravel(), minlength=E))])
+    toks = covering_tokens(offs, srt, k, seed=1)
+    hit = np.isin(srt // k, toks)
+    for e in range(E):
+        a, b = offs[e], offs[e + 1]
+        if b > a:
+            assert hit[a] and hit[b - 1]
+            for r0 in range(a, b, 128):
+                assert hit[r0:min(b, r0 + 128)].any()
+    assert len(toks) < T // 4

@@ -23,7 +23,7 @@ Recipes (all seeded, all bf16 bit patterns stored as uint16):
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 
 import numpy as np
 import torch
@@ -254,6 +254,20 @@ def offload_stack(shape: MoEShape, L: int, T: int, steps: int, seed: int,
     xs = [[px[(s * L + l) % n] for l in range(L)] for s in range(steps)]
     lg = [[pl[(s * L + l) % n] for l in range(L)] for s in range(steps)]
     return OffloadStack(shape, L, T, steps, pb, host, xs, lg)
+
+
+def with_inputs(w: Workload, name: str, T: int, x_bits: np.ndarray, logits: np.ndarray,
+                notes: dict | None = None) -> Workload:
+    """The same pool and page table with another batch of inputs (no copy of the pool)."""
+    return replace(w, name=name, T=T, x_bits=x_bits, logits=logits,
+                   notes={**w.notes, **(notes or {})})
+
+
+def q3_prefill_inputs(seed: int = 0, T: int = 8192, gamma: float = 0.5):
+    """x and logits of q3_prefill_zipf without building its pool (which equals
+    q3_decode's pool at the same seed and pool size)."""
+    x = make_x(seed, T, Q3.H)
+    return x, make_logits(seed, x, Q3.E, bias=zipf_bias(seed, Q3.E, 1.1, gamma))
 
 
 # Named configurations -------------------------------------------------------------
