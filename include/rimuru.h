@@ -209,6 +209,20 @@ int rimuru_view_set_moe_shape(rimuru_view_t view, int layers, int experts, int h
                               int top_k, int renorm);
 
 /*
+ * Batches of at most `max_tokens` tokens run the layer's decode path: three
+ * kernels in place of five, for decode steps of one to a few tokens, where
+ * each routed expert has a row or two and the layer is bound by its weight
+ * bytes and by latency.  The path also needs T * top_k <= 64, the batch's x
+ * rows within 32 KiB (T * hidden * 2) and its h within 96 KiB
+ * (T * top_k * inter * 2); other batches take the general path whatever
+ * `max_tokens` says.  0 turns the decode path off.  Default 0; at most 8.
+ * RIMURU_ERR_ARG outside [0, 8].  The results of the two paths agree within
+ * the layer's bf16 rounding, not bit for bit (their sums run in another
+ * order).  Not thread-safe against a concurrent forward on the same view.
+ */
+int rimuru_view_set_decode_tokens(rimuru_view_t view, int max_tokens);
+
+/*
  * Expert page table entry (explainer page, memory-manager paragraph: each
  * tensor type keeps a page table of its own; paragraph on the fused MoE
  * kernel: the kernel reads an expert's pages in place).  Maps projection `proj` (RIMURU_PROJ_W1/W3/W2) of `expert` in
@@ -252,10 +266,14 @@ typedef struct rimuru_ws_layout {
   uint64_t ptiles;     /* int32 [max_tiles][2]: (expert, first row) of each 256-row pair of blocks */
   uint64_t num_ptiles; /* int32: number of valid pair entries */
   uint64_t tile_cnt;   /* int32 [2][...]: split-K tile counters of the two GEMMs */
-  uint64_t part;       /* fp32 split-K partial tiles (empty when no GEMM is split) */
+  uint64_t part;       /* fp32 partials: split-K tiles of the general path, or the
+                          decode path's GEMM 1 partials (empty when neither runs) */
   uint64_t total;      /* bytes needed */
   int32_t chunks;      /* number of routing chunks */
   int32_t max_tiles;   /* capacity of the tile table */
+  uint64_t plan;       /* int32 [1 + 3 * 64]: the decode path's routed experts (count,
+                          then expert ids, first sorted rows, row counts); empty region
+                          when the batch cannot take the decode path */
 } rimuru_ws_layout;
 
 int rimuru_moe_workspace_layout(rimuru_view_t view, int num_tokens, rimuru_ws_layout* out);
@@ -284,8 +302,10 @@ int rimuru_moe_workspace_layout(rimuru_view_t view, int num_tokens, rimuru_ws_la
  *               intermediates described by rimuru_moe_workspace_layout()
  *   stream      cudaStream_t as void*
  * Every (layer, expert, projection) of `layer` must be mapped
- * (RIMURU_ERR_UNMAPPED otherwise).  Host-side checks run before any launch;
- * kernel-side problems set the device error word and never trap.
+ * (RIMURU_ERR_UNMAPPED otherwise).  The current device must be the one that
+ * holds the pool (and the view's device state, once created): RIMURU_ERR_ARG
+ * otherwise.  Host-side checks run before any launch; kernel-side problems set
+ * the device error word and never trap.
  * CUDA graphs: the first forward after the view's mappings change copies the
  * page table to the device and may wait for an earlier copy; any other
  * forward only launches kernels on `stream` (with programmatic dependent
@@ -342,9 +362,11 @@ int rimuru_moe_forward_host(const void* x_host, const float* logits_host, int nu
  * until the process exits.  It holds the routing tables, the sorted
  * activations, h, y, this layer's page table and an error word; the call
  * makes no cudaMalloc, cudaFree, cudaMallocHost or other allocating call.
- * A forward whose workspace (rimuru_moe_workspace_bytes) plus 8.25 KiB does
- * not fit is rejected with RIMURU_ERR_WORKSPACE before anything is launched
- * (about 370 tokens at hidden 2048 / inter 768 / top-8).
+ * A forward whose workspace (rimuru_moe_workspace_bytes) plus 10 KiB (1 KiB
+ * of alignment slack, the error word's 1 KiB, 8 KiB of page table) does not
+ * fit is rejected with RIMURU_ERR_WORKSPACE before anything is launched
+ * (about 370 tokens at hidden 2048 / inter 768 / top-8).  The workspace part
+ * starts on a 1 KiB boundary, as the ordinary forward requires.
  * First call on a device: it looks up the array's device address
  * (cudaGetSymbolAddress) with that device current and caches it; make that
  * first call before any stream capture.
@@ -354,8 +376,11 @@ int rimuru_moe_forward_host(const void* x_host, const float* logits_host, int nu
  * array: serialise them (one stream, or synchronise between streams).
  * Arguments are those of rimuru_moe_forward without the workspace, plus
  * dev_error: an optional device int that receives the first RIMURU_DEV_*
- * code a kernel reports (the caller zeroes it); NULL keeps errors in the
- * scratch, where they are not reported.
+ * code a kernel reports (the caller zeroes it).  With dev_error NULL, error
+ * reporting is off: the kernels record into a word of the scratch that no
+ * call reads back, so a bad input (a non-finite logit) is not reported.
+ * RIMURU_ERR_ARG when the current device is not the one that holds the pool;
+ * num_tokens must be in [0, 2^20].
  */
 int rimuru_moe_forward_noalloc(const void* x_bf16, const float* logits, int num_tokens,
                                rimuru_view_t view, int layer, void* out_bf16, int* dev_error,
@@ -476,13 +501,17 @@ int rimuru_get_device_error(rimuru_view_t view, int* code, int clear);
 
 /* ------------------------------------------------------------- profiling */
 
-/* Kernel slots of one forward.  When its T * top_k assignments fit one CTA
- * (at most 1024), a forward launches the kernel in slot
- * RIMURU_K_ROUTE_ALIGN_GATHER (routing, grouping and the gather of x rows),
- * then GEMM 1, GEMM 2 and combine; otherwise route, align, GEMM 1 (which
- * gathers its rows from x itself), GEMM 2 and combine.  No current launch
- * sequence uses slot RIMURU_K_GATHER (a separate gather kernel); the slot
- * keeps the numbering of the others and always reports 0 launches. */
+/* Kernel slots of one forward.  A decode-sized batch (see
+ * rimuru_view_set_decode_tokens) launches RIMURU_K_DECODE_GEMM1 (routing in
+ * every CTA, GEMM 1 partials, W2 pages prefetched into L2),
+ * RIMURU_K_DECODE_REDUCE (h) and RIMURU_K_DECODE_GEMM2 (GEMM 2 and the
+ * combine).  Otherwise, when its T * top_k assignments fit one CTA (at most
+ * 1024), a forward launches the kernel in slot RIMURU_K_ROUTE_ALIGN_GATHER
+ * (routing, grouping and the gather of x rows), then GEMM 1, GEMM 2 and
+ * combine; beyond that route, align, GEMM 1 (which gathers its rows from x
+ * itself), GEMM 2 and combine.  No current launch sequence uses slot
+ * RIMURU_K_GATHER (a separate gather kernel); the slot keeps the numbering
+ * of the others and always reports 0 launches. */
 enum {
   RIMURU_K_ROUTE = 0,
   RIMURU_K_ALIGN = 1,
@@ -491,7 +520,10 @@ enum {
   RIMURU_K_GEMM2 = 4,
   RIMURU_K_COMBINE = 5,
   RIMURU_K_ROUTE_ALIGN_GATHER = 6,
-  RIMURU_K_COUNT = 7
+  RIMURU_K_DECODE_GEMM1 = 7,
+  RIMURU_K_DECODE_REDUCE = 8,
+  RIMURU_K_DECODE_GEMM2 = 9,
+  RIMURU_K_COUNT = 10
 };
 
 /* Name of kernel slot `k` ("moe_route", ...), or NULL. */

@@ -19,8 +19,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "librimuru.so")
 
-SOURCES = ["pool.cpp", "forward.cu", "layer.cu", "moe_small.cu", "moe_gemm.cu", "moe_gemm_2sm.cu", "moe_gemm_wide.cu", "noalloc.cu", "selftest.cu", "offload.cu"]
-HEADERS = ["internal.h", "kernels.h", "device.cuh"]
+SOURCES = ["pool.cpp", "forward.cu", "layer.cu", "moe_small.cu", "moe_gemm.cu", "moe_gemm_2sm.cu", "moe_gemm_wide.cu", "moe_decode.cu", "noalloc.cu", "selftest.cu", "offload.cu"]
+HEADERS = ["internal.h", "kernels.h", "device.cuh", "route.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           f"-I{os.path.join(ROOT, 'include')}"]

@@ -117,6 +117,22 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int c0, in
                : "memory");
 }
 
+// L2 prefetch of `bytes` contiguous bytes of global memory (address and size
+// multiples of 16): no shared memory, no barrier, nothing to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// 16 bytes from global memory through the non-coherent path, not kept in L1
+// (read-only data that the CTA reads once).
+__device__ __forceinline__ uint4 ld_nc_na_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // ------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy through the L1-bypassing path (generic proxy).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {

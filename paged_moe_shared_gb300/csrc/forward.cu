@@ -90,8 +90,13 @@ void layout_for(const View& v, int T, rimuru_ws_layout* L) {
   const uint64_t units = std::max<uint64_t>(s1 > 1 ? t1 * s1 : 0, s2 > 1 ? t2 * s2 : 0);
   L->ptiles = take(max_tiles * 2 * 4);
   L->num_ptiles = take(16);
-  L->tile_cnt = take(2 * std::max<uint64_t>(t1, t2) * 4);
-  L->part = take(units * part_rows * 256 * 4);
+  L->tile_cnt = take((2 * std::max<uint64_t>(t1, t2) + kSchedCounters) * 4);
+  // the decode path's fp32 partials share the region (only one path runs per forward)
+  const uint64_t dec = decode_path_fits(T, v.top_k, v.hidden, v.inter)
+                           ? decode_part_bytes(T, v.top_k, v.experts, v.inter)
+                           : 0;
+  L->part = take(std::max<uint64_t>(units * part_rows * 256 * 4, dec));
+  L->plan = take(dec ? kDecodePlanInts * 4 : 0);
   L->total = at;
   L->chunks = chunks;
   L->max_tiles = static_cast<int32_t>(max_tiles);
@@ -185,6 +190,28 @@ int wait_table_upload(View* v) {
   return RIMURU_OK;
 }
 
+int check_device(View* v, int device) {
+  Pool* pool = v->pool;
+  int pd = pool->device.load(std::memory_order_acquire);
+  if (pd == -2) {
+    cudaPointerAttributes at{};
+    pd = -1;
+    if (cudaPointerGetAttributes(&at, pool->base) != cudaSuccess)
+      cudaGetLastError();  // not a pointer CUDA knows of: clear the error this call left
+    else if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged)
+      pd = at.device;
+    pool->device.store(pd, std::memory_order_release);
+  }
+  if (pd >= 0 && pd != device)
+    return fail(RIMURU_ERR_ARG, "the pool lives on device " + std::to_string(pd) +
+                                    " but device " + std::to_string(device) + " is current");
+  if (v->dev && v->dev->device != device)
+    return fail(RIMURU_ERR_ARG, "the view's device state lives on device " +
+                                    std::to_string(v->dev->device) + " but device " +
+                                    std::to_string(device) + " is current");
+  return RIMURU_OK;
+}
+
 void destroy_device_state(View* v) {
   DeviceState* d = v->dev;
   if (!d) return;
@@ -232,9 +259,10 @@ int rimuru_device_sm_count(void) {
 }
 
 const char* rimuru_kernel_name(int k) {
-  static const char* names[RIMURU_K_COUNT] = {"moe_route",        "moe_align", "moe_gather",
-                                              "moe_gemm1_swiglu", "moe_gemm2", "moe_combine",
-                                              "moe_route_align_gather"};
+  static const char* names[RIMURU_K_COUNT] = {
+      "moe_route",         "moe_align",         "moe_gather",       "moe_gemm1_swiglu",
+      "moe_gemm2",         "moe_combine",       "moe_route_align_gather",
+      "moe_decode_gemm1",  "moe_decode_reduce", "moe_decode_gemm2"};
   return (k >= 0 && k < RIMURU_K_COUNT) ? names[k] : nullptr;
 }
 
@@ -265,7 +293,12 @@ int rimuru_moe_forward(const void* x_bf16, const float* logits, int num_tokens, 
   if (workspace_bytes < L.total)
     return fail(RIMURU_ERR_WORKSPACE, "workspace needs " + std::to_string(L.total) + " bytes");
 
-  int st = rimuru::ensure_device_state(&v);
+  int cur = 0;
+  cudaError_t ce = cudaGetDevice(&cur);
+  if (ce != cudaSuccess) return fail(RIMURU_ERR_CUDA, rimuru::cuda_msg("cudaGetDevice", ce));
+  int st = rimuru::check_device(&v, cur);
+  if (st != RIMURU_OK) return st;
+  st = rimuru::ensure_device_state(&v);
   if (st != RIMURU_OK) return st;
   rimuru::DeviceState* d = v.dev;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -289,6 +322,9 @@ int rimuru_moe_forward(const void* x_bf16, const float* logits, int num_tokens, 
   a.err = d->d_err;
   a.tm_w13 = &d->tm_w13;
   a.tm_w2 = &d->tm_w2;
+  a.pool = static_cast<uint8_t*>(v.pool->base);
+  a.page_bytes = v.page_bytes;
+  a.decode_max_tokens = v.decode_max_tokens;
   a.stream = stream;
   a.sm_count = rimuru::sm_count_of(d->device);
   if (a.sm_count <= 0) return fail(RIMURU_ERR_CUDA, "could not query the SM count");

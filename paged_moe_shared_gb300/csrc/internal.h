@@ -2,6 +2,7 @@
 // (forward.cu).  Not part of the public ABI.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <memory>
 #include <mutex>
@@ -12,6 +13,8 @@
 #include "../../include/rimuru.h"
 
 namespace rimuru {
+
+constexpr int kDefaultDecodeTokens = 0;
 
 // Thread-local error message, returned by rimuru_last_error().
 int fail(int status, const std::string& msg);
@@ -40,6 +43,9 @@ struct Pool {
   int next_view_id = 1;
   bool any_placed = false;
   std::mutex mu;
+  // Device that holds the pool bytes: -2 = not looked up yet, -1 = unknown (the
+  // pointer is not a device allocation CUDA knows of; no check is made).
+  std::atomic<int> device{-2};
 
   int level_of(uint64_t page_bytes) const;  // -1 if none
   int add_level(uint64_t page_bytes);       // keeps the chain ordered; returns its index
@@ -66,6 +72,8 @@ struct View {
   // MoE shape (set once)
   bool has_shape = false;
   int layers = 0, experts = 0, hidden = 0, inter = 0, top_k = 0, renorm = 1;
+  // batches of at most this many tokens take the three-kernel decode path
+  int decode_max_tokens = kDefaultDecodeTokens;
   std::vector<int32_t> page_table;       // [layers][experts][3], -1 = unmapped
   std::vector<int32_t> mapped_per_layer;  // number of mapped entries per layer
   std::vector<int32_t> map_count;        // per page: how many entries point at it
@@ -75,6 +83,9 @@ struct View {
 };
 
 void destroy_device_state(View* v);
+// RIMURU_OK when `device` (the caller's current device) holds the view's pool
+// and, once the view has device state, that state; RIMURU_ERR_ARG otherwise.
+int check_device(View* v, int device);
 // Block until the last page-table upload has left the host staging copy.
 int wait_table_upload(View* v);
 

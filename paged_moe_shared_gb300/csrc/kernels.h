@@ -27,6 +27,10 @@ constexpr int kPrefetchKBlocks = 16;
 // kMinSplitBlocks k blocks per split (shorter splits cost more in the
 // pipeline fill and the reduction than they save).
 constexpr int kSplitTarget = 304;
+// Work-unit counters after the split-K tile counters (zeroed with them by the
+// kernel that writes the tile tables): [0] feeds the 256-row GEMM 1's dynamic
+// unit scheduler.
+constexpr int kSchedCounters = 2;
 constexpr int kMinSplitBlocks = 8;
 inline int split_count(long long tiles_ub, int nkb) {
   if (tiles_ub <= 0 || tiles_ub * 4 > kSplitTarget) return 1;
@@ -105,6 +109,9 @@ struct GemmArgs {
   int prefetch_kb;
   int prefetch_bpe;
   int num_experts;
+  // Dynamic scheduling (256-row GEMM 1): units after the first gridDim.x are
+  // taken from this counter, zero when the kernel starts.
+  int32_t* sched;
 };
 
 // a3: h = silu(x_sorted w1_e) * (x_sorted w3_e); w1/w3 read in place from pages.
@@ -141,6 +148,45 @@ cudaError_t launch_gemm2(const CUtensorMap& tm_h, const CUtensorMap& tm_w2, cons
 cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv, const float* w, int T,
                            int k, int H, __nv_bfloat16* out, const LaunchOpts& o);
 
+// ------------------------------------------------ decode-sized batches
+// Batches of at most kDecodeMaxT tokens and kDecodeMaxA assignments (and whose
+// x rows and h fit the kernels' shared memory, decode_path_fits) may run as
+// three kernels: decode_gemm1 (routing in every CTA, W1/W3 streamed in
+// balanced k-block units with fp32 partials, W2 pages prefetched into L2),
+// decode_reduce (h from the partials) and decode_gemm2 (y from L2-resident W2
+// and the combine).
+constexpr int kDecodeMaxT = 8;
+constexpr int kDecodeMaxA = 64;
+constexpr int kDecodeGridMax = 160;     // decode_gemm1 CTAs at most (sizes the partials)
+constexpr int kDecodeStagesMax = 12;    // ring stages of 16 KiB
+constexpr int kDecodeMaxHBytes = 98304;  // h of the batch in decode_gemm2's shared memory
+constexpr int kDecodePlanInts = 1 + 3 * kDecodeMaxA;
+
+struct DecodeArgs {
+  const float* logits;          // [T][E]
+  const __nv_bfloat16* x;       // [T][H]
+  int T, E, k, renorm, H, I;
+  const int32_t* page_table;    // [E][3] of the layer
+  int num_pages;
+  const uint8_t* pool;          // pool base: W2 pages are read (and prefetched) by address
+  uint64_t page_bytes;
+  int32_t *ids, *sorted, *inv, *offsets, *tiles, *num_tiles, *ptiles, *num_ptiles, *plan;
+  float* w;
+  float* part;                  // fp32 partials, [groups + grid1 slots][T][128]
+  __nv_bfloat16 *h, *y, *out;   // h [A][I], y [A][H] in sorted order; out [T][H]
+  int* err;
+  int grid1;                    // CTAs of decode_gemm1
+  int stages;                   // set by the launcher
+  int prefetch_w2;              // 1: decode_gemm1 prefetches the routed W2 pages into L2
+};
+
+bool decode_path_fits(int T, int k, int H, int I);
+int decode_grid1(int sm_count);
+uint64_t decode_part_bytes(int T, int k, int E, int I);
+cudaError_t launch_decode_gemm1(const CUtensorMap& tm_w13, DecodeArgs a, const LaunchOpts& o);
+cudaError_t launch_decode_reduce(DecodeArgs a, const LaunchOpts& o);
+cudaError_t launch_decode_gemm2(DecodeArgs a, const LaunchOpts& o);
+
 // bf16 TMA descriptor with 128-byte swizzle (dims and box innermost first,
 // strides in bytes for dims 1..rank-1).  Returns a rimuru status.
 int make_bf16_map(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims,
@@ -165,6 +211,9 @@ struct LayerLaunch {
   cudaStream_t stream = nullptr;
   int sm_count = 0;
   bool pdl = true;
+  uint8_t* pool = nullptr;          // pool base (the decode path reads W2 pages by address)
+  uint64_t page_bytes = 0;
+  int decode_max_tokens = 0;        // batches of at most this many tokens take the decode path
   cudaEvent_t* ev = nullptr;        // 2 * RIMURU_K_COUNT events, or null
   unsigned ev_mask = 0;             // kernels bracketed by their event pair
   unsigned* hits = nullptr;         // bit k set when kernel k was launched between its events

@@ -143,7 +143,7 @@ int launch_layer_route(const LayerLaunch& a) {
   if (e == cudaSuccess)
     e = launch_align(q.ids, q.chunk_hist, a.layout.chunks, a.T * a.k, a.E, tpc * a.k, q.offsets,
                      q.sorted, q.inv, q.tiles, q.num_tiles, q.ptiles, q.num_ptiles, q.tile_cnt,
-                     static_cast<int>(2 * std::max(splits_of(a).t1, splits_of(a).t2)), a.err, next);
+                     static_cast<int>(2 * std::max(splits_of(a).t1, splits_of(a).t2) + kSchedCounters), a.err, next);
   mark(RIMURU_K_ALIGN, 1);
   if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, cuda_msg("kernel launch", e));
   return RIMURU_OK;
@@ -190,6 +190,7 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   g1.ldx = H;
   g2.splits = sp.s2;
   g2.tile_cnt = q.tile_cnt + std::max(sp.t1, sp.t2);
+  g1.sched = q.tile_cnt + 2 * std::max(sp.t1, sp.t2);
   g1.out = q.h;
   g1.ldo = I;
   g1.n_blocks = I / 128;
@@ -268,7 +269,67 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   return RIMURU_OK;
 }
 
+// Decode-sized batches: decode_gemm1 -> decode_reduce -> decode_gemm2.
+int launch_layer_decode(const LayerLaunch& a) {
+  const rimuru_ws_layout& L = a.layout;
+  const LayerPtrs q = pointers_of(a);
+  DecodeArgs d{};
+  d.logits = a.logits;
+  d.x = static_cast<const __nv_bfloat16*>(a.x);
+  d.T = a.T;
+  d.E = a.E;
+  d.k = a.k;
+  d.renorm = a.renorm;
+  d.H = a.H;
+  d.I = a.I;
+  d.page_table = a.table;
+  d.num_pages = a.num_pages;
+  d.pool = a.pool;
+  d.page_bytes = a.page_bytes;
+  d.ids = q.ids;
+  d.w = q.w;
+  d.sorted = q.sorted;
+  d.inv = q.inv;
+  d.offsets = q.offsets;
+  d.tiles = q.tiles;
+  d.num_tiles = q.num_tiles;
+  d.ptiles = q.ptiles;
+  d.num_ptiles = q.num_ptiles;
+  d.plan = reinterpret_cast<int32_t*>(a.ws + L.plan);
+  d.part = q.part;
+  d.h = q.h;
+  d.y = q.y;
+  d.out = static_cast<__nv_bfloat16*>(a.out);
+  d.err = a.err;
+  d.grid1 = decode_grid1(a.sm_count);
+  d.prefetch_w2 = 1;
+  LaunchOpts o;
+  o.stream = a.stream;
+  o.sm_count = a.sm_count;
+  o.pdl = a.pdl;
+  cudaError_t e = cudaSuccess;
+  auto mark = [&](int kidx, int which) {
+    if (a.ev && (a.ev_mask >> kidx & 1u) && e == cudaSuccess) {
+      e = cudaEventRecord(a.ev[kidx * 2 + which], a.stream);
+      if (which == 1 && a.hits) *a.hits |= 1u << kidx;
+    }
+  };
+  mark(RIMURU_K_DECODE_GEMM1, 0);
+  if (e == cudaSuccess) e = launch_decode_gemm1(*a.tm_w13, d, o);
+  mark(RIMURU_K_DECODE_GEMM1, 1);
+  mark(RIMURU_K_DECODE_REDUCE, 0);
+  if (e == cudaSuccess) e = launch_decode_reduce(d, o);
+  mark(RIMURU_K_DECODE_REDUCE, 1);
+  mark(RIMURU_K_DECODE_GEMM2, 0);
+  if (e == cudaSuccess) e = launch_decode_gemm2(d, o);
+  mark(RIMURU_K_DECODE_GEMM2, 1);
+  if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, cuda_msg("kernel launch", e));
+  return RIMURU_OK;
+}
+
 int launch_layer(const LayerLaunch& a) {
+  if (a.T <= a.decode_max_tokens && a.pool && decode_path_fits(a.T, a.k, a.H, a.I))
+    return launch_layer_decode(a);
   if (static_cast<long long>(a.T) * a.k > kChunkAssign) {
     int st = launch_layer_route(a);
     if (st != RIMURU_OK) return st;
@@ -291,7 +352,7 @@ int launch_layer(const LayerLaunch& a) {
     e = launch_route_align_gather(
         a.logits, static_cast<const __nv_bfloat16*>(a.x), a.T, a.E, a.k, a.renorm, a.H, q.ids, q.w,
         q.offsets, q.sorted, q.inv, q.tiles, q.num_tiles, q.ptiles, q.num_ptiles, q.tile_cnt,
-        static_cast<int>(2 * std::max(splits_of(a).t1, splits_of(a).t2)), q.xs, a.err, first);
+        static_cast<int>(2 * std::max(splits_of(a).t1, splits_of(a).t2) + kSchedCounters), q.xs, a.err, first);
   if (prof && e == cudaSuccess) {
     e = cudaEventRecord(a.ev[kidx * 2 + 1], a.stream);
     if (a.hits) *a.hits |= 1u << kidx;

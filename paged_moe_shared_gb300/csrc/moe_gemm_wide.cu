@@ -59,12 +59,21 @@ constexpr int kSmemBytes = kStages * kStageBytes + kEpiWarps * kStageOutBytes +
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 static_assert(kThreads * 128 <= 65536, "registers: 128 per thread fit one SM");
 
+// Dynamic unit scheduling: the producer takes each next unit from a global
+// counter (units differ in cost: an expert's lone last block is half a tile)
+// and publishes it in a small ring read by every other role in the same order.
+constexpr int kSched = 4;
+constexpr int kSchedReaders = 1 + kEpiWarps + kLoaderWarps;  // MMA thread + one per warp
+
 struct Shared {
   uint64_t full[kStages];   // weight bytes + one arrival per loader thread
   uint64_t empty[kStages];  // the stage's MMAs are done
   uint64_t tfull;           // both accumulator halves hold the tile
   uint64_t tempty[2];       // half h drained by the eight epilogue warps
   uint64_t drain;
+  uint64_t sfull[kSched];   // unit index published
+  uint64_t sempty[kSched];  // every role has read it
+  int sunit[kSched];
   uint32_t tmem_base;
   int abort;
 };
@@ -95,6 +104,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh->tempty[0], kEpiWarps);
     mbar_init(&sh->tempty[1], kEpiWarps);
     mbar_init(&sh->drain, 1);
+    for (int i = 0; i < kSched; ++i) {
+      mbar_init(&sh->sfull[i], 1);
+      mbar_init(&sh->sempty[i], kSchedReaders);
+    }
     sh->abort = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_w);
@@ -119,7 +132,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = p.weights_evict_first ? policy_evict_first() : policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+      int u = blockIdx.x;
+      for (int i = 0; ok; ++i) {
+        // publish unit u as this CTA's i-th (u >= n_units ends every role's loop)
+        const uint32_t sl = i % kSched, sph = (i / kSched) & 1u;
+        if (!mbar_wait(&sh->sempty[sl], sph ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        sh->sunit[sl] = u;
+        mbar_arrive(&sh->sfull[sl]);
+        if (u >= n_units) break;
+        // the next unit, fetched while this one's copies are issued
+        const int next = static_cast<int>(gridDim.x) + atomicAdd(p.sched, 1);
         const int pt = u / p.n_blocks, nb = u % p.n_blocks;
         const int e = p.tiles[2 * pt];
         int pg0 = p.page_table[3 * e + RIMURU_PROJ_W1];
@@ -142,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(b + 2 * kBChunk, &tm_w, &sh->full[s], n0, kb * BK, pg1, pol_w);
           tma_load_3d(b + 3 * kBChunk, &tm_w, &sh->full[s], n0 + 64, kb * BK, pg1, pol_w);
         }
+        u = next;
       }
       if (!ok) fail(sh, p.err);
       // every copy this thread issued must have landed before the CTA exits
@@ -156,7 +182,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true);
       uint32_t it = 0, local = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++local) {
+      for (;; ++local) {
+        const uint32_t sl = local % kSched, sph = (local / kSched) & 1u;
+        if (!mbar_wait(&sh->sfull[sl], sph, abort)) {
+          ok = false;
+          break;
+        }
+        const int u = sh->sunit[sl];
+        mbar_arrive(&sh->sempty[sl]);
+        if (u >= n_units) break;
         const int pt = u / p.n_blocks;
         const int e = p.tiles[2 * pt], row0 = p.tiles[2 * pt + 1];
         const bool has1 = p.offsets[e + 1] - row0 > BM;
@@ -230,7 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub = lane >> 3, chunk = lane & 7;
     uint32_t it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+    for (uint32_t i = 0; ok; ++i) {
+      const uint32_t sl = i % kSched, sph = (i / kSched) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sh->sfull[sl], sph, abort))) {
+        ok = false;
+        break;
+      }
+      const int u = sh->sunit[sl];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->sempty[sl]);
+      if (u >= n_units) break;
       const int pt = u / p.n_blocks;
       const int e = p.tiles[2 * pt];
       const int hrow0 = p.tiles[2 * pt + 1] + half * BM;  // first row of this warp's half
@@ -272,8 +315,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                  // TMEM lane quadrant this warp may read
     const int cb = 64 * ((warp - 2) >> 2);   // this warp's first output column of the block
     const uint32_t blk_s = smem_u32(sOut + (warp - 2) * kStageOutBytes);
-    uint32_t local = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++local) {
+    for (uint32_t local = 0;; ++local) {
+      const uint32_t sl = local % kSched, sph = (local / kSched) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sh->sfull[sl], sph, abort))) {
+        if (lane == 0) fail(sh, p.err);
+        break;
+      }
+      const int u = sh->sunit[sl];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->sempty[sl]);
+      if (u >= n_units) break;
       const bool got = mbar_wait(&sh->tfull, local & 1u, abort);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) fail(sh, p.err);

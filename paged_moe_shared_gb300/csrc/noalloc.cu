@@ -22,8 +22,15 @@ namespace rimuru {
 namespace {
 
 constexpr uint64_t kNoAllocScratchBytes = 16ull << 20;  // 16 MiB per device
-constexpr uint64_t kErrBytes = 256;                     // device error word
-constexpr uint64_t kTableBytes = 8192;                  // one layer: experts * 3 int32 (<= 512 experts)
+// Layout from the first 1 KiB boundary of the array (the array itself is only
+// 256-byte aligned): the error word's 1 KiB, then 8 KiB for one layer's page
+// table (experts * 3 int32, at most 512 experts), then the layer's workspace,
+// whose regions are 1 KiB-aligned offsets from a 1 KiB-aligned base as in the
+// ordinary forward.
+constexpr uint64_t kAlignSlack = 1024;
+constexpr uint64_t kErrBytes = 1024;
+constexpr uint64_t kTableBytes = 8192;
+constexpr uint64_t kHeaderBytes = kAlignSlack + kErrBytes + kTableBytes;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
@@ -65,7 +72,8 @@ extern "C" int rimuru_moe_forward_noalloc(const void* x_bf16, const float* logit
   View& v = view->v;
   if (!v.has_shape) return fail(RIMURU_ERR_STATE, "view has no MoE shape");
   if (layer < 0 || layer >= v.layers) return fail(RIMURU_ERR_RANGE, "layer out of range");
-  if (num_tokens < 0) return fail(RIMURU_ERR_ARG, "negative token count");
+  if (num_tokens < 0 || num_tokens > (1 << 20))
+    return fail(RIMURU_ERR_ARG, "num_tokens must be in [0, 2^20]");
   if (v.mapped_per_layer[layer] != v.experts * 3)
     return fail(RIMURU_ERR_UNMAPPED, "layer " + std::to_string(layer) + " has unmapped projections");
   if (num_tokens == 0) return RIMURU_OK;
@@ -79,7 +87,7 @@ extern "C" int rimuru_moe_forward_noalloc(const void* x_bf16, const float* logit
   rimuru_ws_layout L;
   int st = rimuru_moe_workspace_layout(view, num_tokens, &L);
   if (st != RIMURU_OK) return st;
-  const uint64_t need = kErrBytes + kTableBytes + L.total;
+  const uint64_t need = kHeaderBytes + L.total;
   if (need > kNoAllocScratchBytes)
     return fail(RIMURU_ERR_WORKSPACE,
                 std::to_string(num_tokens) + " tokens need " + std::to_string(need) +
@@ -91,6 +99,8 @@ extern "C" int rimuru_moe_forward_noalloc(const void* x_bf16, const float* logit
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return fail(RIMURU_ERR_CUDA, msg_of("cudaGetDevice", e));
+  st = check_device(&v, device);
+  if (st != RIMURU_OK) return st;
   uint8_t* scratch = nullptr;
   st = scratch_for_device(device, &scratch);
   if (st != RIMURU_OK) return st;
@@ -99,9 +109,11 @@ extern "C" int rimuru_moe_forward_noalloc(const void* x_bf16, const float* logit
   if (e != cudaSuccess || sms <= 0) return fail(RIMURU_ERR_CUDA, "could not query the SM count");
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  int* err = dev_error ? dev_error : reinterpret_cast<int*>(scratch);
-  int32_t* table = reinterpret_cast<int32_t*>(scratch + kErrBytes);
-  uint8_t* ws = scratch + kErrBytes + kTableBytes;  // 256-byte aligned base
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(scratch) + kAlignSlack - 1) & ~static_cast<uintptr_t>(kAlignSlack - 1));
+  int* err = dev_error ? dev_error : reinterpret_cast<int*>(base);
+  int32_t* table = reinterpret_cast<int32_t*>(base + kErrBytes);
+  uint8_t* ws = base + kErrBytes + kTableBytes;  // 1 KiB-aligned, as the ordinary forward requires
 
   const int T = num_tokens, E = v.experts, k = v.top_k, H = v.hidden, I = v.inter;
   // Left over from the previous call: the scratch error word (cleared here) and
@@ -134,6 +146,9 @@ extern "C" int rimuru_moe_forward_noalloc(const void* x_bf16, const float* logit
   a.err = err;
   a.tm_w13 = &tm_w13;
   a.tm_w2 = &tm_w2;
+  a.pool = static_cast<uint8_t*>(v.pool->base);
+  a.page_bytes = v.page_bytes;
+  a.decode_max_tokens = v.decode_max_tokens;
   a.stream = stream;
   a.sm_count = sms;
   return launch_layer(a);

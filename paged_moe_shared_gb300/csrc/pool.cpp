@@ -436,6 +436,14 @@ int rimuru_page_owned(rimuru_view_t view, int64_t page_id, int* owned) {
   return RIMURU_OK;
 }
 
+int rimuru_view_set_decode_tokens(rimuru_view_t view, int max_tokens) {
+  rimuru::clear_error();
+  if (!view) return fail(RIMURU_ERR_ARG, "null view");
+  if (max_tokens < 0 || max_tokens > 8) return fail(RIMURU_ERR_ARG, "max_tokens must be in [0, 8]");
+  view->v.decode_max_tokens = max_tokens;
+  return RIMURU_OK;
+}
+
 int rimuru_view_set_moe_shape(rimuru_view_t view, int layers, int experts, int hidden, int inter,
                               int top_k, int renorm) {
   rimuru::clear_error();

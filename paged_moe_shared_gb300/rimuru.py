@@ -28,7 +28,8 @@ ERR_UNSUPPORTED = -10
 PROJ_W1, PROJ_W3, PROJ_W2 = 0, 1, 2
 NEW_GROUP = -2
 DEV_OK, DEV_BAD_PAGE, DEV_NONFINITE, DEV_TIMEOUT, DEV_BAD_SHAPE = 0, 1, 2, 3, 4
-K_ROUTE, K_ALIGN, K_GATHER, K_GEMM1, K_GEMM2, K_COMBINE, K_ROUTE_ALIGN_GATHER, K_COUNT = range(8)
+(K_ROUTE, K_ALIGN, K_GATHER, K_GEMM1, K_GEMM2, K_COMBINE, K_ROUTE_ALIGN_GATHER, K_DECODE_GEMM1,
+ K_DECODE_REDUCE, K_DECODE_GEMM2, K_COUNT) = range(11)
 
 # Every symbol include/rimuru.h declares.
 EXPORTS = [
@@ -36,6 +37,7 @@ EXPORTS = [
     "rimuru_huge_page_bytes", "rimuru_pool_num_levels", "rimuru_pool_level_stats",
     "rimuru_view_create", "rimuru_view_destroy", "rimuru_view_info", "rimuru_page_alloc",
     "rimuru_page_place", "rimuru_page_free", "rimuru_page_owned", "rimuru_view_set_moe_shape",
+    "rimuru_view_set_decode_tokens",
     "rimuru_expert_map", "rimuru_expert_unmap", "rimuru_expert_lookup",
     "rimuru_moe_workspace_bytes", "rimuru_moe_workspace_layout", "rimuru_moe_forward",
     "rimuru_moe_forward_noalloc", "rimuru_moe_host_workspace_bytes", "rimuru_moe_forward_host",
@@ -65,7 +67,8 @@ class LevelStats(ctypes.Structure):
 class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "ids", "weights", "chunk_hist", "offsets", "sorted", "inv", "tiles", "num_tiles",
-        "x_sorted", "h", "y", "ptiles", "num_ptiles", "tile_cnt", "part", "total")] + [("chunks", ctypes.c_int32), ("max_tiles", ctypes.c_int32)]
+        "x_sorted", "h", "y", "ptiles", "num_ptiles", "tile_cnt", "part", "total")] + [
+        ("chunks", ctypes.c_int32), ("max_tiles", ctypes.c_int32), ("plan", ctypes.c_uint64)]
 
 
 class OffloadCounters(ctypes.Structure):
@@ -96,6 +99,7 @@ def _load():
         "rimuru_page_free": ([P, i64], i32),
         "rimuru_page_owned": ([P, i64, ctypes.POINTER(i32)], i32),
         "rimuru_view_set_moe_shape": ([P, i32, i32, i32, i32, i32, i32], i32),
+        "rimuru_view_set_decode_tokens": ([P, i32], i32),
         "rimuru_expert_map": ([P, i32, i32, i32, i64], i32),
         "rimuru_expert_unmap": ([P, i32, i32, i32], i32),
         "rimuru_expert_lookup": ([P, i32, i32, i32, ctypes.POINTER(i64)], i32),
@@ -227,6 +231,10 @@ def rimuru_page_owned(view, page_id: int) -> bool:
 def rimuru_view_set_moe_shape(view, layers: int, experts: int, hidden: int, inter: int,
                               top_k: int, renorm: bool = True) -> None:
     _check(lib.rimuru_view_set_moe_shape(view, layers, experts, hidden, inter, top_k, int(renorm)))
+
+
+def rimuru_view_set_decode_tokens(view, max_tokens: int) -> None:
+    _check(lib.rimuru_view_set_decode_tokens(view, max_tokens))
 
 
 def rimuru_expert_map(view, layer: int, expert: int, proj: int, page_id: int) -> None:

@@ -24,9 +24,11 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 class Runner:
     """A workload placed on the device once; ``forward`` can be called repeatedly."""
 
-    def __init__(self, w, device=DEV):
+    def __init__(self, w, device=DEV, decode_tokens=None):
         self.w = w
         self.pool, self.ev, self.kv = load_workload(w, device)
+        if decode_tokens is not None:  # batches up to this size take the decode path (0: never)
+            R.rimuru_view_set_decode_tokens(self.ev, decode_tokens)
         self.x = bf16_tensor(w.x_bits, device)
         self.logits = torch.from_numpy(np.ascontiguousarray(w.logits)).to(device)
         self.out = torch.empty_like(self.x)
@@ -80,3 +82,43 @@ def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
     if not np.isfinite(got).all():
         return float("inf")
     return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def covering_tokens(offsets: np.ndarray, sorted_: np.ndarray, k: int, seed: int,
+                    block: int = 128) -> np.ndarray:
+    """Tokens to check when a layer is too large for the oracle to compute in full.
+
+    The sample is chosen so that the checked assignment rows (every row of every chosen
+    token) include, for each expert that received tokens, its first and last row in the
+    expert-sorted order and at least one row of each of its ``block``-row blocks: every
+    GEMM tile (both halves of a 256-row pair, an expert's lone last block, every column
+    block and every k block, since a checked row spans them all) is then compared.
+    ``offsets`` / ``sorted_`` are the oracle's grouping of the full batch."""
+    rng = np.random.default_rng(seed)
+    A = sorted_.size
+    covered = np.zeros(A, bool)
+    tok_of_row = sorted_ // k
+    # rows of every token: row_of[f] = position of assignment f in the sorted order
+    row_of = np.empty(A, np.int64)
+    row_of[sorted_] = np.arange(A)
+    chosen = set()
+
+    def take(row):
+        t = int(tok_of_row[row])
+        if t not in chosen:
+            chosen.add(t)
+            covered[row_of[t * k:(t + 1) * k]] = True
+
+    E = offsets.size - 1
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            take(a)
+            take(b - 1)
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        for r0 in range(a, b, block):
+            r1 = min(b, r0 + block)
+            if not covered[r0:r1].any():
+                take(int(rng.integers(r0, r1)))
+    return np.array(sorted(chosen), dtype=np.int64)

@@ -179,3 +179,20 @@ def test_capacity_below_one_layer_is_rejected():
     with pytest.raises(R.RimuruError) as e:
         run_stack(st, cap=3, prefetch=False)
     assert e.value.status == R.ERR_OOM
+
+
+def test_qwen3_shaped_stack_matches_oracle_and_lru_model():
+    """Three layers of the Qwen3-30B-A3B shape at full size (3 MiB pages, so the merged
+    adjacent host-to-pool copies and the per-layer page-table slice from the pinned ring run
+    on real page sizes), 64 tokens, two steps, with 200 experts resident: one cycle of layers
+    routes to about 378 experts, so experts are evicted and loaded again in every step, and
+    a prefetch of layer l + 1 competes with layer l's own experts.  Every token of every
+    layer against the oracle; the counters against the model of least-recently-used
+    eviction (the stack configuration's policy)."""
+    st = wl.offload_stack(wl.Q3, L=3, T=64, steps=2, seed=61, distinct_layers=1)
+    counters, expected, worst = run_stack(st, cap=200, prefetch=True)
+    assert counters == expected
+    # least-recently-used eviction over a cycle larger than the cache evicts exactly what is
+    # needed next, so the model (and the cache) report misses, prefetches and no hits
+    assert counters["evictions"] > 0 and counters["misses"] > 0
+    assert counters["prefetch_loads"] > 0

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import workloads as wl
-from gpu_harness import Runner, rel_err
+from gpu_harness import Runner, covering_tokens, rel_err
 from oracle import Oracle
 
 pytestmark = pytest.mark.gpu
@@ -64,8 +64,8 @@ def run_oracle(oracle, w, tokens=None, hidden=True):
                               s.renorm, tokens=tokens, want_hidden=hidden)
 
 
-def run_gpu(w):
-    r = Runner(w)
+def run_gpu(w, decode_tokens=None):
+    r = Runner(w, decode_tokens=decode_tokens)
     try:
         r.forward()
         return r.results()
@@ -208,27 +208,57 @@ def zipf_exponent(counts, ranks):
     return -np.polyfit(np.log(ranks[nz]), np.log(counts[nz]), 1)[0]
 
 
+def sample_covering(oracle, w, seed):
+    """Routing and grouping of the whole batch from the oracle, then a token sample whose
+    assignment rows reach every 128-row block of every expert and each expert's first and
+    last row (so every GEMM tile is compared, not a random subset of them)."""
+    s = w.shape
+    ids, _ = oracle.route(w.logits, s.k, s.renorm)
+    srt, offs = oracle.align(ids, s.E)
+    return covering_tokens(offs, srt, s.k, seed)
+
+
+def assert_rows_cover_every_block(res, tokens, k):
+    """Every 128-row block of every expert holds a checked row, and so do the first and
+    last rows of every expert (read back from the GPU's own grouping)."""
+    rows = np.nonzero(np.isin(res["sorted"] // k, tokens))[0]
+    hit = np.zeros(res["sorted"].size, bool)
+    hit[rows] = True
+    offs = res["offsets"]
+    for e in range(offs.size - 1):
+        a, b = int(offs[e]), int(offs[e + 1])
+        if b > a:
+            assert hit[a] and hit[b - 1], e
+            for r0 in range(a, b, 128):
+                assert hit[r0:min(b, r0 + 128)].any(), (e, r0)
+
+
 def test_q3_prefill_zipf_sampled(oracle):
     """8192 prefill tokens with Zipf(1.1)-skewed routing: routing, permutation and tiles for
-    all tokens; h, y and out for 48 sampled tokens (the oracle computes them one by one)."""
+    all tokens; h, y and out for a token sample that reaches every row block of every
+    expert (the oracle computes those tokens one by one)."""
     w = wl.q3_prefill_zipf(0)
-    tokens = np.sort(np.random.default_rng(0).choice(w.T, 48, replace=False))
+    tokens = sample_covering(oracle, w, 0)
     o = run_oracle(oracle, w, tokens=tokens)
     counts = np.diff(o["offsets"])
     s = zipf_exponent(counts, wl.zipf_ranks(0, w.shape.E))
     assert 0.9 <= s <= 1.3, f"realised popularity exponent {s:.2f}"
-    check(run_gpu(w), w, o, tokens=tokens)
+    res = run_gpu(w)
+    assert_rows_cover_every_block(res, tokens, w.shape.k)
+    check(res, w, o, tokens=tokens)
 
 
 def test_q3_prefill_heavy_skew_sampled(oracle):
     """A steeper bias (gamma 2): 38 of 128 experts get every assignment, the rest are empty,
     and the hottest expert holds all 8192 tokens (64 row blocks)."""
     w = wl.q3_prefill_zipf(0, gamma=2.0)
-    tokens = np.sort(np.random.default_rng(2).choice(w.T, 32, replace=False))
+    tokens = sample_covering(oracle, w, 2)
     o = run_oracle(oracle, w, tokens=tokens)
     counts = np.diff(o["offsets"])
     assert (counts == 0).sum() >= 1 and counts.max() == w.T
-    check(run_gpu(w), w, o, tokens=tokens)
+    res = run_gpu(w)
+    assert_rows_cover_every_block(res, tokens, w.shape.k)
+    check(res, w, o, tokens=tokens)
 
 
 @pytest.mark.parametrize("T", [1, 16, 256])
@@ -241,8 +271,10 @@ def test_q35_mixed_pool(oracle, T):
 
 def test_q35_mixed_pool_4096_sampled(oracle):
     w = wl.q35_mixed_pool(0, T=4096)
-    tokens = np.sort(np.random.default_rng(1).choice(w.T, 32, replace=False))
-    check(run_gpu(w), w, run_oracle(oracle, w, tokens=tokens), tokens=tokens)
+    tokens = sample_covering(oracle, w, 1)
+    res = run_gpu(w)
+    assert_rows_cover_every_block(res, tokens, w.shape.k)
+    check(res, w, run_oracle(oracle, w, tokens=tokens), tokens=tokens)
 
 
 def _wide_inter_t1():
@@ -266,7 +298,7 @@ def test_split_k_is_used_for_few_tiles_and_is_deterministic(oracle, make):
     """With few tiles the GEMMs split K over several CTAs and sum the fp32 partials in split
     order, so repeated forwards agree bit for bit."""
     w = make()
-    r = Runner(w)
+    r = Runner(w, decode_tokens=0)  # the general path (one token would take the decode path)
     try:
         assert r.layout["total"] > r.layout["part"]  # a partial-sum region exists
         r.forward()
@@ -278,6 +310,16 @@ def test_split_k_is_used_for_few_tiles_and_is_deterministic(oracle, make):
     check(a, w, run_oracle(oracle, w))
     for key in ("out", "h", "y"):
         assert np.array_equal(a[key], b[key]), key
+    from paged_moe_shared_gb300 import rimuru as R
+    r = Runner(w, decode_tokens=0)
+    try:
+        R.rimuru_profile_enable(r.ev, R.PROFILE_ALL, 1)
+        r.forward()
+        r.results()
+        assert R.rimuru_profile_read(r.ev, R.K_DECODE_GEMM1)[0] == 0
+        assert R.rimuru_profile_read(r.ev, R.K_GEMM1)[0] == 1
+    finally:
+        r.close()
 
 
 def test_cta_pair_gemm2_with_odd_and_even_block_counts(oracle):
@@ -294,6 +336,171 @@ def test_cta_pair_gemm2_with_odd_and_even_block_counts(oracle):
     o = run_oracle(oracle, w)
     blocks = (np.diff(o["offsets"]) + 127) // 128
     assert (blocks % 2 == 1).any() and (blocks % 2 == 0).any() and blocks.max() >= 4
+    check(run_gpu(w), w, o)
+
+
+# ------------------------------------------------------------ decode-sized batches
+# Batches of up to the view's decode-token limit take three kernels: GEMM 1 partials over
+# balanced k-block units with routing in every CTA, the reduction to h, and GEMM 2 with the
+# combine.  Each case runs against the oracle, and against the general path on the same
+# inputs (within the bf16 rounding both paths share, not bit for bit).
+def decode_launches(r):
+    from paged_moe_shared_gb300 import rimuru as R
+    R.rimuru_profile_enable(r.ev, R.PROFILE_ALL, 1)
+    r.forward()
+    res = r.results()
+    launched = {R.rimuru_kernel_name(i): R.rimuru_profile_read(r.ev, i)[0] for i in range(R.K_COUNT)}
+    R.rimuru_profile_enable(r.ev, 0, 1)
+    return res, launched
+
+
+DECODE = {
+    "q3_t1": lambda: wl.q3_decode(0, T=1),
+    "q3_t2": lambda: wl.q3_decode(1, T=2),
+    "q3_t4": lambda: wl.q3_decode(2, T=4),
+    "q35_t1": lambda: wl.q35_mixed_pool(1, T=1),
+    "q35_t2": lambda: wl.q35_mixed_pool(2, T=2),
+    "q35_t4": lambda: wl.q35_mixed_pool(3, T=4),
+    "tiny_t1": lambda: wl.tiny(4, T=1),
+    "tiny_t3": lambda: wl.tiny(5, T=3),
+    # 64 assignments (the most the path takes) over 64 experts, E past one warp's lanes
+    "k32_t2": lambda: wl.build_simple("k32_t2", wl.MoEShape(H=256, I=128, E=64, k=32), 2,
+                                      pool_pages=200, seed=6),
+    # 512 experts (16 logits per lane in the routing warp), k = 10
+    "e512_k10_t4": lambda: wl.build_simple("e512", wl.MoEShape(H=1024, I=256, E=512, k=10), 4,
+                                           pool_pages=1540, seed=7),
+    # 32 KiB of x rows (the most the path stages) and 24 column blocks of h
+    "h4096_i1536_t4": lambda: wl.build_simple("h4096", wl.MoEShape(H=4096, I=1536, E=32, k=4), 4,
+                                              pool_pages=100, seed=8),
+    # every token routed to the same expert (4 rows in one unit)
+    "one_expert_t4": lambda: wl.build_simple(
+        "hot", wl.TINY, 4, pool_pages=64, seed=9,
+        logits=np.tile(np.array([[0, 0, 9, 0, 0, 0, 8, 0]], np.float32), (4, 1))),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DECODE))
+def test_decode_path_against_oracle_and_general_path(oracle, name):
+    w = DECODE[name]()
+    r = Runner(w, decode_tokens=8)
+    try:
+        res, launched = decode_launches(r)
+        r.forward()
+        again = r.results()
+    finally:
+        r.close()
+    assert launched["moe_decode_gemm1"] == 1 and launched["moe_decode_reduce"] == 1
+    assert launched["moe_decode_gemm2"] == 1
+    assert sum(launched.values()) == 3
+    o = run_oracle(oracle, w, hidden=True)
+    check(res, w, o)
+    for key in ("out", "h", "y", "ids", "w", "sorted", "inv"):  # deterministic
+        assert np.array_equal(res[key], again[key]), key
+    res2 = run_gpu(w, decode_tokens=0)
+    check(res2, w, o)
+    assert rel_err(res["out"], res2["out"]) <= TOL
+
+
+def test_decode_path_nonfinite_logits_raise_the_device_error():
+    from paged_moe_shared_gb300 import rimuru as R
+    w = wl.tiny(24, T=2)
+    w.logits[1, 4] = np.inf
+    res = run_gpu(w, decode_tokens=8)
+    assert res["dev_err"] == R.DEV_NONFINITE
+    assert ((res["ids"] >= 0) & (res["ids"] < w.shape.E)).all()
+
+
+def test_decode_path_token_limit_setting(oracle):
+    """rimuru_view_set_decode_tokens moves the boundary between the two paths (up to 8
+    tokens), 0 turns the decode path off, and values outside [0, 8] are rejected."""
+    from paged_moe_shared_gb300 import rimuru as R
+    w = wl.q35_mixed_pool(6, T=8)
+    o = run_oracle(oracle, w)
+    for limit, expect in ((8, True), (7, False), (0, False)):
+        r = Runner(w, decode_tokens=limit)
+        try:
+            res, launched = decode_launches(r)
+        finally:
+            r.close()
+        assert (launched["moe_decode_gemm1"] == 1) == expect, limit
+        check(res, w, o)
+    r = Runner(wl.tiny(1, T=1))
+    try:
+        for bad in (-1, 9):
+            with pytest.raises(R.RimuruError) as e:
+                R.rimuru_view_set_decode_tokens(r.ev, bad)
+            assert e.value.status == R.ERR_ARG
+    finally:
+        r.close()
+
+
+def test_decode_path_replays_from_a_cuda_graph():
+    """One-token forwards recorded by stream capture replay to the bits of plain forwards,
+    on the recorded inputs and on new ones written into the same buffers."""
+    import torch
+
+    from paged_moe_shared_gb300 import rimuru as R
+    w = wl.q35_mixed_pool(7, T=1)
+    r = Runner(w, decode_tokens=8)
+    try:
+        s = torch.cuda.Stream()
+        r.forward(s)
+        s.synchronize()
+        plain = r.out.clone()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            r.forward(s)
+        r.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(r.out, plain)
+        w2 = wl.q35_mixed_pool(8, T=1)
+        r.x.copy_(torch.from_numpy(w2.x_bits.view(np.int16)).view(torch.bfloat16))
+        r.logits.copy_(torch.from_numpy(w2.logits))
+        g.replay()
+        torch.cuda.synchronize()
+        replayed = r.out.clone()
+        r.forward(s)
+        s.synchronize()
+        assert torch.equal(replayed, r.out)
+        assert R.rimuru_get_device_error(r.ev) == R.DEV_OK
+    finally:
+        r.close()
+
+
+# ------------------------------------------------------ activation and routing extremes
+# Weights scaled so that the gate pre-activation g spans about +-100: silu(g) saturates to g
+# on the positive side, and below g = -87 the exponential in 1 + e^-g overflows fp32, where
+# silu must give 0 (times the up value), not NaN.  Router logits of magnitude ~1e3 make the
+# top-k softmax weights one-hot to within fp32 (the lower slots underflow to 0 or to
+# subnormals).  Each case takes another GEMM path: the small-batch kernel with TMA rows,
+# split-K, the gathered 128-row GEMM 1, and the 256-row / CTA-pair GEMMs.
+EXTREME = {
+    "decode_t4": (wl.TINY, 4, 2.5),
+    "small_batch_t64": (wl.TINY, 64, 2.5),
+    "split_k_h1024_t16": (wl.MoEShape(H=1024, I=128, E=8, k=2), 16, 1.25),
+    "gathered_t600": (wl.TINY, 600, 2.5),
+    "wide_pair_t1500": (wl.TINY, 1500, 2.5),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EXTREME))
+def test_silu_saturation_and_large_logits(oracle, name):
+    shape, T, std = EXTREME[name]
+    seed = 31
+    x = wl.make_x(seed, T, shape.H)
+    logits = wl.make_logits(seed, x, shape.E, gate_std=60.0)
+    assert np.abs(logits).max() > 1e3
+    weights = wl.make_expert_weights(seed, shape, std=std)
+    w = wl.build_simple("extreme_" + name, shape, T, pool_pages=3 * shape.E + 8, seed=seed,
+                        weights=weights, x_bits=x, logits=logits)
+    o = run_oracle(oracle, w, hidden=True)
+    # the gate pre-activations of the routed pairs reach both tails
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    g = np.stack([xf[t] @ wl.bf16_bits_to_f32(weights[0][e]).astype(np.float64)
+                  for t, e in zip(np.repeat(np.arange(T), shape.k), o["ids"].ravel())])
+    assert g.min() < -87.5 and g.max() > 87.5, (g.min(), g.max())
+    assert (o["w"].max(axis=1) > 0.999).mean() > 0.5  # mostly one-hot routing weights
     check(run_gpu(w), w, o)
 
 
