@@ -215,8 +215,8 @@ int rimuru_view_set_moe_shape(rimuru_view_t view, int layers, int experts, int h
  * bytes and by latency.  The path also needs T * top_k <= 64, the batch's x
  * rows within 32 KiB (T * hidden * 2) and its h within 96 KiB
  * (T * top_k * inter * 2); other batches take the general path whatever
- * `max_tokens` says.  0 turns the decode path off.  Default 0; at most 8.
- * RIMURU_ERR_ARG outside [0, 8].  The results of the two paths agree within
+ * `max_tokens` says.  0 turns the decode path off.  Default 0; at most 4.
+ * RIMURU_ERR_ARG outside [0, 4].  The results of the two paths agree within
  * the layer's bf16 rounding, not bit for bit (their sums run in another
  * order).  Not thread-safe against a concurrent forward on the same view.
  */

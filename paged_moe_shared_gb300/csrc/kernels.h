@@ -155,7 +155,7 @@ cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv, const flo
 // balanced k-block units with fp32 partials, W2 pages prefetched into L2),
 // decode_reduce (h from the partials) and decode_gemm2 (y from L2-resident W2
 // and the combine).
-constexpr int kDecodeMaxT = 8;
+constexpr int kDecodeMaxT = 4;
 constexpr int kDecodeMaxA = 64;
 constexpr int kDecodeGridMax = 160;     // decode_gemm1 CTAs at most (sizes the partials)
 constexpr int kDecodeStagesMax = 12;    // ring stages of 16 KiB

@@ -375,11 +375,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
         case 1: mac_unit<1>(box, xs, tok, H, hoff, hq, lane, acc); break;
         case 2: mac_unit<2>(box, xs, tok, H, hoff, hq, lane, acc); break;
         case 3: mac_unit<3>(box, xs, tok, H, hoff, hq, lane, acc); break;
-        case 4: mac_unit<4>(box, xs, tok, H, hoff, hq, lane, acc); break;
-        case 5: mac_unit<5>(box, xs, tok, H, hoff, hq, lane, acc); break;
-        case 6: mac_unit<6>(box, xs, tok, H, hoff, hq, lane, acc); break;
-        case 7: mac_unit<7>(box, xs, tok, H, hoff, hq, lane, acc); break;
-        default: mac_unit<8>(box, xs, tok, H, hoff, hq, lane, acc); break;
+        default: mac_unit<4>(box, xs, tok, H, hoff, hq, lane, acc); break;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->empty[s]);
@@ -543,18 +539,10 @@ __global__ void __launch_bounds__(kThreads2, RMAX <= 2 ? 2 : 1) decode_gemm2_ker
       y_rows<1>(w2, hs, uoff, I, H, c0, lane, p.y, s_y);
     } else if (RMAX == 2 || rows == 2) {
       y_rows<(RMAX >= 2 ? 2 : 1)>(w2, hs, uoff, I, H, c0, lane, p.y, s_y);
-    } else if (rows <= 4 || RMAX <= 4) {
-      switch (rows) {
-        case 3: y_rows<(RMAX >= 3 ? 3 : 1)>(w2, hs, uoff, I, H, c0, lane, p.y, s_y); break;
-        default: y_rows<(RMAX >= 4 ? 4 : 1)>(w2, hs, uoff, I, H, c0, lane, p.y, s_y); break;
-      }
+    } else if (rows == 3) {
+      y_rows<(RMAX >= 3 ? 3 : 1)>(w2, hs, uoff, I, H, c0, lane, p.y, s_y);
     } else {
-      switch (rows) {
-        case 5: y_rows<(RMAX >= 5 ? 5 : 1)>(w2, hs, uoff, I, H, c0, lane, p.y, s_y); break;
-        case 6: y_rows<(RMAX >= 6 ? 6 : 1)>(w2, hs, uoff, I, H, c0, lane, p.y, s_y); break;
-        case 7: y_rows<(RMAX >= 7 ? 7 : 1)>(w2, hs, uoff, I, H, c0, lane, p.y, s_y); break;
-        default: y_rows<(RMAX >= 8 ? 8 : 1)>(w2, hs, uoff, I, H, c0, lane, p.y, s_y); break;
-      }
+      y_rows<(RMAX >= 4 ? 4 : 1)>(w2, hs, uoff, I, H, c0, lane, p.y, s_y);
     }
   }
   __syncthreads();
@@ -669,8 +657,7 @@ cudaError_t launch_decode_gemm2(DecodeArgs a, const LaunchOpts& o) {
   // an expert's rows are at most T (each token picks an expert once)
   if (a.T <= 1) return launch_gemm2_rmax<1>(a, o);
   if (a.T <= 2) return launch_gemm2_rmax<2>(a, o);
-  if (a.T <= 4) return launch_gemm2_rmax<4>(a, o);
-  return launch_gemm2_rmax<8>(a, o);
+  return launch_gemm2_rmax<4>(a, o);  // T <= kDecodeMaxT = 4
 }
 
 }  // namespace rimuru

@@ -439,7 +439,7 @@ int rimuru_page_owned(rimuru_view_t view, int64_t page_id, int* owned) {
 int rimuru_view_set_decode_tokens(rimuru_view_t view, int max_tokens) {
   rimuru::clear_error();
   if (!view) return fail(RIMURU_ERR_ARG, "null view");
-  if (max_tokens < 0 || max_tokens > 8) return fail(RIMURU_ERR_ARG, "max_tokens must be in [0, 8]");
+  if (max_tokens < 0 || max_tokens > 4) return fail(RIMURU_ERR_ARG, "max_tokens must be in [0, 4]");
   view->v.decode_max_tokens = max_tokens;
   return RIMURU_OK;
 }

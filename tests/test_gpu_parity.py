@@ -382,7 +382,7 @@ DECODE = {
 @pytest.mark.parametrize("name", sorted(DECODE))
 def test_decode_path_against_oracle_and_general_path(oracle, name):
     w = DECODE[name]()
-    r = Runner(w, decode_tokens=8)
+    r = Runner(w, decode_tokens=4)
     try:
         res, launched = decode_launches(r)
         r.forward()
@@ -405,18 +405,18 @@ def test_decode_path_nonfinite_logits_raise_the_device_error():
     from paged_moe_shared_gb300 import rimuru as R
     w = wl.tiny(24, T=2)
     w.logits[1, 4] = np.inf
-    res = run_gpu(w, decode_tokens=8)
+    res = run_gpu(w, decode_tokens=4)
     assert res["dev_err"] == R.DEV_NONFINITE
     assert ((res["ids"] >= 0) & (res["ids"] < w.shape.E)).all()
 
 
 def test_decode_path_token_limit_setting(oracle):
-    """rimuru_view_set_decode_tokens moves the boundary between the two paths (up to 8
-    tokens), 0 turns the decode path off, and values outside [0, 8] are rejected."""
+    """rimuru_view_set_decode_tokens moves the boundary between the two paths (up to 4
+    tokens), 0 turns the decode path off, and values outside [0, 4] are rejected."""
     from paged_moe_shared_gb300 import rimuru as R
-    w = wl.q35_mixed_pool(6, T=8)
+    w = wl.q35_mixed_pool(6, T=3)
     o = run_oracle(oracle, w)
-    for limit, expect in ((8, True), (7, False), (0, False)):
+    for limit, expect in ((4, True), (3, True), (2, False), (0, False)):
         r = Runner(w, decode_tokens=limit)
         try:
             res, launched = decode_launches(r)
@@ -426,7 +426,7 @@ def test_decode_path_token_limit_setting(oracle):
         check(res, w, o)
     r = Runner(wl.tiny(1, T=1))
     try:
-        for bad in (-1, 9):
+        for bad in (-1, 5):
             with pytest.raises(R.RimuruError) as e:
                 R.rimuru_view_set_decode_tokens(r.ev, bad)
             assert e.value.status == R.ERR_ARG
@@ -441,7 +441,7 @@ def test_decode_path_replays_from_a_cuda_graph():
 
     from paged_moe_shared_gb300 import rimuru as R
     w = wl.q35_mixed_pool(7, T=1)
-    r = Runner(w, decode_tokens=8)
+    r = Runner(w, decode_tokens=4)
     try:
         s = torch.cuda.Stream()
         r.forward(s)
