@@ -339,6 +339,30 @@ def test_cta_pair_gemm2_with_odd_and_even_block_counts(oracle):
     check(run_gpu(w), w, o)
 
 
+def test_cta_pair_gemm2_partial_last_pairs_of_every_kind(oracle):
+    """An expert's last pair of row blocks on the CTA-pair GEMM 2 (and the 256-row GEMM 1)
+    holds 1 to 256 of its rows; the rows after them belong to the next expert and must not
+    be overwritten.  Router logits fix each expert's row count so that the last pairs hold
+    1, 16, 17, 255, 256 (a full pair), 129, 128 and 150 rows: a lone block of one row, lone
+    blocks ending on and just past a 16-row boundary, full and ragged second blocks."""
+    shape = wl.TINY
+    T = 1500
+    counts = [257, 16, 529, 511, 256, 385, 128, 918]
+    assert sum(counts) == T * shape.k and max(counts) <= T
+    slots = np.repeat(np.arange(shape.E), counts)
+    x = wl.make_x(23, T, shape.H)
+    logits = (-2.0 + 0.1 * np.random.default_rng(23).standard_normal((T, shape.E))).astype(np.float32)
+    logits[np.arange(T), slots[:T]] = 4.0
+    logits[np.arange(T), slots[T:]] = 3.0
+    w = wl.build_simple("tiny_partial_pairs", shape, T, pool_pages=64, seed=23, x_bits=x,
+                        logits=logits)
+    o = run_oracle(oracle, w)
+    assert np.diff(o["offsets"]).tolist() == counts
+    last = [c - 256 * ((c - 1) // 256) for c in counts]
+    assert last == [1, 16, 17, 255, 256, 129, 128, 150]
+    check(run_gpu(w), w, o)
+
+
 # ------------------------------------------------------------ decode-sized batches
 # Batches of up to the view's decode-token limit take three kernels: GEMM 1 partials over
 # balanced k-block units with routing in every CTA, the reduction to h, and GEMM 2 with the
