@@ -132,13 +132,16 @@ cudaError_t launch_gemm1_swiglu_gather(const CUtensorMap& tm_w13, const GemmArgs
 // tiles of the pair table (tiles/num_tiles in `a` name it) on one SM, two
 // M = 128 MMAs per k step sharing the staged weights, A rows gathered from x
 // like launch_gemm1_swiglu_gather.  No split-K.
-cudaError_t launch_gemm1_wide(const CUtensorMap& tm_w13, const GemmArgs& a, const LaunchOpts& o);
+// tm_h maps a.out (h) in 32-row x 64-column boxes for the epilogue's TMA stores.
+cudaError_t launch_gemm1_wide(const CUtensorMap& tm_w13, const CUtensorMap& tm_h,
+                              const GemmArgs& a, const LaunchOpts& o);
 
 // a4 for large batches on CTA pairs (tcgen05 cta_group::2): a tile is one
 // entry of the pair table (tiles/num_tiles in `a` name it) times one column
-// block; each CTA stages half of every weight tile.
-cudaError_t launch_gemm2_pair(const CUtensorMap& tm_h, const CUtensorMap& tm_w2, const GemmArgs& a,
-                              const LaunchOpts& o);
+// block; each CTA stages half of every weight tile.  tm_y maps a.out (y) in
+// 32-row x 64-column boxes for the epilogue's TMA stores.
+cudaError_t launch_gemm2_pair(const CUtensorMap& tm_h, const CUtensorMap& tm_w2,
+                              const CUtensorMap& tm_y, const GemmArgs& a, const LaunchOpts& o);
 
 // a4: y = h w2_e; w2 read in place from its page.
 cudaError_t launch_gemm2(const CUtensorMap& tm_h, const CUtensorMap& tm_w2, const GemmArgs& a,

@@ -154,7 +154,7 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   const LayerPtrs q = pointers_of(a);
   const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I;
   const int A = T * k;
-  CUtensorMap tm_x{}, tm_h;
+  CUtensorMap tm_x{}, tm_h, tm_h_st, tm_y;
   if (gathered) {  // x_sorted exists (and is read by GEMM 1) only behind the small-batch kernel
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(A)};
     cuuint64_t str[1] = {static_cast<cuuint64_t>(H) * 2};
@@ -167,6 +167,16 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
     cuuint64_t str[1] = {static_cast<cuuint64_t>(I) * 2};
     cuuint32_t box[2] = {64, 128};
     int st = make_bf16_map(&tm_h, q.h, 2, dims, str, box);
+    if (st != RIMURU_OK) return st;
+    cuuint32_t box_st[2] = {64, 32};  // the 256-row GEMM 1's stores
+    st = make_bf16_map(&tm_h_st, q.h, 2, dims, str, box_st);
+    if (st != RIMURU_OK) return st;
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(A)};
+    cuuint64_t str[1] = {static_cast<cuuint64_t>(H) * 2};
+    cuuint32_t box[2] = {64, 32};
+    int st = make_bf16_map(&tm_y, q.y, 2, dims, str, box);
     if (st != RIMURU_OK) return st;
   }
   GemmArgs g1{};
@@ -247,7 +257,7 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
       GemmArgs w1 = g1;  // 256-row tiles from the pair table
       w1.tiles = q.ptiles;
       w1.num_tiles = q.num_ptiles;
-      e = launch_gemm1_wide(*a.tm_w13, w1, o1);
+      e = launch_gemm1_wide(*a.tm_w13, tm_h_st, w1, o1);
     } else {
       e = launch_gemm1_swiglu_gather(*a.tm_w13, g1, o1);
     }
@@ -256,7 +266,7 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   mark(RIMURU_K_GEMM2, 0);
   if (e == cudaSuccess) {
     if (pairs && sp.s2 == 1)
-      e = launch_gemm2_pair(tm_h, *a.tm_w2, p2, o);
+      e = launch_gemm2_pair(tm_h, *a.tm_w2, tm_y, p2, o);
     else
       e = launch_gemm2(tm_h, *a.tm_w2, g2, o);
   }

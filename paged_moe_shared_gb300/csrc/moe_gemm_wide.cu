@@ -84,7 +84,8 @@ __device__ __forceinline__ void fail(Shared* sh, int* err) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    wide_gemm1_kernel(const __grid_constant__ CUtensorMap tm_w, const GemmArgs p) {
+    wide_gemm1_kernel(const __grid_constant__ CUtensorMap tm_w,
+                      const __grid_constant__ CUtensorMap tm_out, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -111,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh->abort = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_out);
   }
   if (warp == 1) {
     tmem_alloc(&sh->tmem_base, kTmemCols);
@@ -358,13 +360,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->tempty[h]);
         if (rows > 0) {
-          // lane l holds row q*32 + l: stage it, then store four whole rows per instruction
+          // lane l holds row q*32 + l: stage it, then one TMA store of the block, or,
+          // when it holds rows of the next expert, four whole rows per store instruction
+          if (lane == 0) bulk_wait_read_all();  // an earlier block's TMA store has read it
+          __syncwarp();
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint32_t at = blk_s + lane * 128 + ((c ^ (lane & 7)) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(at), "r"(packed[4 * c]),
                          "r"(packed[4 * c + 1]), "r"(packed[4 * c + 2]), "r"(packed[4 * c + 3])
                          : "memory");
+          }
+          if (rows - q * 32 >= 32) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm_out, blk_s, n0, row0 + h * BM + q * 32);
+              bulk_commit();
+            }
+            continue;
           }
           __syncwarp();
           const int chunk = lane & 7;
@@ -387,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (warp >= 2 && warp < 2 + kEpiWarps && lane == 0) bulk_wait_all();  // h is complete
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -397,7 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_gemm1_wide(const CUtensorMap& tm_w13, const GemmArgs& a, const LaunchOpts& o) {
+cudaError_t launch_gemm1_wide(const CUtensorMap& tm_w13, const CUtensorMap& tm_h,
+                              const GemmArgs& a, const LaunchOpts& o) {
   // the shared-memory opt-in is a per-device function attribute: set it once per device
   static std::atomic<bool> configured[64];
   int dev = 0;
@@ -422,7 +438,7 @@ cudaError_t launch_gemm1_wide(const CUtensorMap& tm_w13, const GemmArgs& a, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = o.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, wide_gemm1_kernel, tm_w13, a);
+  return cudaLaunchKernelEx(&cfg, wide_gemm1_kernel, tm_w13, tm_h, a);
 }
 
 }  // namespace rimuru
