@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
           const int chunk = lane & 7;
-#pragma unroll
+#pragma unroll 1  // blocks with rows of the next expert only; unrolled, the kernel spills
           for (int i = 0; i < 8; ++i) {
             const int rr = 4 * i + (lane >> 3);  // row within this warp's 32
             uint4 val;
