@@ -288,9 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           src[i] = p.x + static_cast<size_t>(p.sorted[hrow0 + r] / p.top_k) * p.ldx + chunk * 8;
         }
       }
-      // x (T x H, a few tens of MB) is gathered k times per column block; kept in
-      // L2 ahead of the streamed weights it is not re-read from DRAM between the
-      // tiles that gather the same rows (prefill GEMM 1 317 -> 311 us).
+      // x (T x H, a few tens of MB) is gathered k times per column block: the
+      // row copies carry the same L2 evict-last priority as the weight boxes
+      // (prefill GEMM 1 317 -> 311 us; its DRAM traffic did not change).
       const uint64_t pol_x = policy_evict_last();
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
