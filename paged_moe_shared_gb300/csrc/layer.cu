@@ -154,7 +154,12 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
   const LayerPtrs q = pointers_of(a);
   const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I;
   const int A = T * k;
-  CUtensorMap tm_x{}, tm_h, tm_h_st, tm_y;
+  CUtensorMap tm_x{}, tm_h, tm_h_st{}, tm_y{};
+  // Large batches (at least two 128-row blocks per expert on average) run
+  // GEMM 1 as 256-row tiles and GEMM 2 on CTA pairs over the table of 256-row
+  // pairs of blocks; their epilogues store 32-row boxes of h and y by TMA.
+  const bool pairs = static_cast<long long>(A) >=
+                     static_cast<long long>(kPairMinBlocksPerExpert) * kTileM * E;
   if (gathered) {  // x_sorted exists (and is read by GEMM 1) only behind the small-batch kernel
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(A)};
     cuuint64_t str[1] = {static_cast<cuuint64_t>(H) * 2};
@@ -168,11 +173,11 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
     cuuint32_t box[2] = {64, 128};
     int st = make_bf16_map(&tm_h, q.h, 2, dims, str, box);
     if (st != RIMURU_OK) return st;
-    cuuint32_t box_st[2] = {64, 32};  // the 256-row GEMM 1's stores
-    st = make_bf16_map(&tm_h_st, q.h, 2, dims, str, box_st);
+    cuuint32_t box_st[2] = {64, 32};
+    if (pairs) st = make_bf16_map(&tm_h_st, q.h, 2, dims, str, box_st);
     if (st != RIMURU_OK) return st;
   }
-  {
+  if (pairs) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(A)};
     cuuint64_t str[1] = {static_cast<cuuint64_t>(H) * 2};
     cuuint32_t box[2] = {64, 32};
@@ -239,10 +244,6 @@ int launch_layer_experts(const LayerLaunch& a, bool after_route, bool gathered) 
     }
   };
   mark(RIMURU_K_GEMM1, 0);
-  // Large batches (at least two 128-row blocks per expert on average) run
-  // GEMM 2 on CTA pairs over the table of 256-row pairs of blocks.
-  const bool pairs = static_cast<long long>(A) >=
-                     static_cast<long long>(kPairMinBlocksPerExpert) * kTileM * E;
   GemmArgs p2 = g2;
   p2.tiles = q.ptiles;
   p2.num_tiles = q.num_ptiles;
