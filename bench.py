@@ -7,7 +7,8 @@ rows, GEMM 2, combine) over one batch of synthetic tokens, through the C ABI on 
 inputs.
 The default workload is the Qwen3-30B-A3B-shaped layer with 64 decode tokens; its expert
 pages (about 1.2 GB touched per step) exceed the 129 MB L2, so no flush is needed between
-steps.  Rank 0 prints one JSON line.  ``--impl reference`` times the CPU oracle on the
+steps.  On one GPU the default line also carries the 8192-token prefill of the same layer, the
+Qwen3.5-shaped layer at 1 / 16 / 256 / 4096 tokens and the 48-layer offloaded stack.  Rank 0 prints one JSON line.  ``--impl reference`` times the CPU oracle on the
 host cores instead (a deliberately slow baseline, not a target).
 """
 from __future__ import annotations
@@ -75,7 +76,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join("/tmp", f"rimuru_clocks_{os.getpid()}.csv")
+        self.path = os.path.join("/tmp", f"rimuru_clocks_{os.getpid()}_{id(self)}.csv")
 
     def start(self):
         try:
@@ -123,7 +124,8 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz),
                 "samples_under_load": len(loaded),
                 "window": "every GPU leg of this run (timed region, bracketed pass, e2e, "
-                          "graph replays, prefill block)"}
+                          "graph replays, and the prefill, sweep and offload blocks of a "
+                          "default one-GPU run)"}
 
 
 def source_digest(*rel_paths):
@@ -685,6 +687,40 @@ def run_ours(args, rank, world, local_rank):
                 pre["gamma_2"] = entry
             Lp.close()
         result["prefill"] = {**pre["gamma_0.5"], "heavy_skew": pre["gamma_2"]}
+
+    # --------------------------------------------- Qwen3.5 sweep and offload blocks
+    # One GPU only (a replica run would multiply the offload stack's 54 GiB of pinned host
+    # memory): the Qwen3.5-shaped layer in a pool shared with KV blocks at 1 / 16 / 256 /
+    # 4096 tokens, and the 48-layer offloaded stack on its configured LRU policy, so that the
+    # default line records them too.
+    if args.workload == "q3_decode" and not args.no_prefill and args.tokens is None \
+            and args.pool_pages is None and world == 1:
+        sweep = {}
+        Ks = min(K, 500)
+        for T in (1, 16, 256, 4096):
+            ws = wl.q35_mixed_pool(args.seed, T=T)
+            nl = layers_to_cycle(ws)
+            Ls = Layer(ws, dev, nl)
+            ms_ = measure(Ls, args, Ks, world, dist, dev, full=False)
+            sroof, slayer, _ = summarise(ms_, peaks)
+            sweep[f"T{T}"] = {"value": round(ms_["value"], 1), "unit": "tokens/s",
+                              "ms_per_step": round(ms_["ms_per_step"], 5), "steps": Ks,
+                              "layers_cycled": nl, "layer_roofline": slayer,
+                              "roofline": {k: sroof[k] for k in ("kernel", "achieved", "frac",
+                                                                 "unit", "bound")},
+                              "gpu_launches": ms_["launches_per_step"] * Ks}
+            Ls.close()
+        result["q35_sweep"] = {"workload": f"q35_mixed_pool: {WORKLOAD_TEXT['q35_mixed_pool']}",
+                               **sweep}
+        try:
+            oargs = argparse.Namespace(**{**vars(args), "steps": 8, "warmup": 3,
+                                          "tokens": None})
+            off = run_offload(oargs, rank, world, local_rank)
+            result["offload"] = {k: off[k] for k in ("metric", "value", "unit", "ms_per_step",
+                                                     "steps", "warmup", "config", "roofline",
+                                                     "cache", "layer_cycle", "gpu_launches")}
+        except Exception as exc:  # host memory for the pinned stack, or the link
+            result["offload"] = {"unavailable": f"{type(exc).__name__}: {exc}"[:300]}
 
     result["clocks"] = clocks.stop()
     if rank == 0 and not args.no_cpu_baseline:
