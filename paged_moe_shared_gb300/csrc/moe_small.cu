@@ -95,53 +95,65 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const float* __restrict
     chunk_hist[static_cast<size_t>(blockIdx.x) * E + e] = s_hist[e];
 }
 
-// Exclusive prefix sum over the block (one value per thread, blockDim <= 1024).
-__device__ int block_exclusive_scan(int v, int* s_warp) {
+// Exclusive prefix sums over the block of three per-thread counts at once
+// (blockDim <= 1024): one scan of a packed 64-bit value, a in bits 0-25, b in
+// 26-44 and c in 45-63, so the block's sums must stay below 2^26, 2^19 and
+// 2^19.  Here a counts assignments (at most 2^25) and b, c the 128-row blocks
+// and pairs of blocks (at most 2^18 + E).  The barriers inside also order the
+// callers' earlier shared-memory writes before their later reads.
+struct Scan3 {
+  int a, b, c;
+};
+__device__ Scan3 block_exclusive_scan3(int a, int b, int c, unsigned long long* s_warp) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  int x = v;
+  const unsigned long long v = static_cast<unsigned long long>(a) |
+                               (static_cast<unsigned long long>(b) << 26) |
+                               (static_cast<unsigned long long>(c) << 45);
+  unsigned long long x = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    int y = __shfl_up_sync(kFull, x, off);
+    const unsigned long long y = __shfl_up_sync(kFull, x, off);
     if (lane >= off) x += y;
   }
   if (lane == 31) s_warp[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int s = lane < nwarps ? s_warp[lane] : 0;
+    unsigned long long t = lane < nwarps ? s_warp[lane] : 0ull;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      int y = __shfl_up_sync(kFull, s, off);
-      if (lane >= off) s += y;
+      const unsigned long long y = __shfl_up_sync(kFull, t, off);
+      if (lane >= off) t += y;
     }
-    if (lane < nwarps) s_warp[lane] = s;  // inclusive warp totals
+    if (lane < nwarps) s_warp[lane] = t;  // inclusive warp totals
   }
   __syncthreads();
-  int before = warp > 0 ? s_warp[warp - 1] : 0;
+  const unsigned long long before = warp > 0 ? s_warp[warp - 1] : 0ull;
   __syncthreads();  // s_warp may be reused by the caller
-  return before + x - v;
+  const unsigned long long ex = before + x - v;
+  return {static_cast<int>(ex & ((1ull << 26) - 1)), static_cast<int>((ex >> 26) & ((1ull << 19) - 1)),
+          static_cast<int>(ex >> 45)};
 }
 
 // Offsets, the 128-row tile table, the table of 256-row pairs of blocks and the
-// zeroed split-K counters, from each expert's count `tot` and exclusive offset
-// `off` (held by thread e of the CTA for e < E).  Every thread of the CTA calls it.
-__device__ void write_tables(int E, int tot, int off, int32_t* __restrict__ offsets,
-                             int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles,
-                             int32_t* __restrict__ ptiles, int32_t* __restrict__ num_ptiles,
-                             int32_t* __restrict__ tile_cnt, int cnt_len, int* s_warp) {
+// zeroed split-K counters, from each expert's count `tot`, its 128-row blocks
+// `nb` and pairs of blocks `np` (the last one possibly alone), and their
+// exclusive prefixes `off`, `first` and `pfirst` (held by thread e of the CTA
+// for e < E).  Every thread of the CTA calls it.
+__device__ void write_tables(int E, int tot, int off, int nb, int first, int np, int pfirst,
+                             int32_t* __restrict__ offsets, int32_t* __restrict__ tiles,
+                             int32_t* __restrict__ num_tiles, int32_t* __restrict__ ptiles,
+                             int32_t* __restrict__ num_ptiles, int32_t* __restrict__ tile_cnt,
+                             int cnt_len) {
   const int tid = threadIdx.x;
   for (int i = tid; i < cnt_len; i += blockDim.x) tile_cnt[i] = 0;
   if (tid < E) offsets[tid] = off;
   if (tid == E - 1) offsets[E] = off + tot;
-  const int nb = tid < E ? (tot + kTileM - 1) / kTileM : 0;
-  const int first = block_exclusive_scan(nb, s_warp);
   for (int b = 0; b < nb; ++b) {
     tiles[2 * (first + b)] = tid;
     tiles[2 * (first + b) + 1] = off + b * kTileM;
   }
   if (tid == E - 1) *num_tiles = first + nb;
-  const int np = (nb + 1) / 2;  // pairs of blocks, the last one possibly alone
-  const int pfirst = block_exclusive_scan(np, s_warp);
   for (int b = 0; b < np; ++b) {
     ptiles[2 * (pfirst + b)] = tid;
     ptiles[2 * (pfirst + b) + 1] = off + b * 2 * kTileM;
@@ -169,7 +181,7 @@ __global__ void __launch_bounds__(kChunkAssign, 2) moe_align_kernel(
   __shared__ int s_part_bef[kChunkAssign];
   __shared__ int s_base[kMaxExperts];
   __shared__ uint16_t s_wh[kChunkAssign / 32][kMaxExperts];  // per-warp counts, then their prefix
-  __shared__ int s_warp[32];
+  __shared__ unsigned long long s_warp[32];
   grid_dep_wait();
   grid_dep_launch();
   const int c = blockIdx.x;
@@ -226,7 +238,10 @@ __global__ void __launch_bounds__(kChunkAssign, 2) moe_align_kernel(
       before += s_part_bef[p * E + tid];
     }
   }
-  const int off = block_exclusive_scan(tot, s_warp);  // also orders the s_wh counts
+  const int nb = tid < E ? (tot + kTileM - 1) / kTileM : 0;
+  const int np = (nb + 1) / 2;
+  const Scan3 sc = block_exclusive_scan3(tot, nb, np, s_warp);  // also orders the s_wh counts
+  const int off = sc.a;
   if (tid < E) {
     s_base[tid] = off + before;
     int acc = 0;  // earlier warps' assignments of expert tid inside this chunk
@@ -237,8 +252,8 @@ __global__ void __launch_bounds__(kChunkAssign, 2) moe_align_kernel(
     }
   }
   if (c == 0)
-    write_tables(E, tot, off, offsets, tiles, num_tiles, ptiles, num_ptiles, tile_cnt, cnt_len,
-                 s_warp);
+    write_tables(E, tot, off, nb, sc.b, np, sc.c, offsets, tiles, num_tiles, ptiles, num_ptiles,
+                 tile_cnt, cnt_len);
   __syncthreads();
   if (my >= 0) {
     const int pos = s_base[my] + s_wh[warp][my] + rank_in;
@@ -277,7 +292,7 @@ __global__ void __launch_bounds__(kChunkAssign) moe_route_align_gather_kernel(
   __shared__ int s_sorted[kChunkAssign];                  // assignment held by sorted row r
   __shared__ uint16_t s_wh[kFusedWarps][kMaxExperts];     // per-warp counts, then their prefix
   __shared__ int s_off[kMaxExperts];
-  __shared__ int s_warp[32];
+  __shared__ unsigned long long s_warp[32];
   grid_dep_wait();
   grid_dep_launch();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -324,11 +339,14 @@ __global__ void __launch_bounds__(kChunkAssign) moe_route_align_gather_kernel(
       tot += v;
     }
   }
-  const int off = block_exclusive_scan(tot, s_warp);
+  const int nb = tid < E ? (tot + kTileM - 1) / kTileM : 0;
+  const int np = (nb + 1) / 2;
+  const Scan3 sc = block_exclusive_scan3(tot, nb, np, s_warp);
+  const int off = sc.a;
   if (tid < E) s_off[tid] = off;
   if (lead)
-    write_tables(E, tot, off, offsets, tiles, num_tiles, ptiles, num_ptiles, tile_cnt, cnt_len,
-                 s_warp);
+    write_tables(E, tot, off, nb, sc.b, np, sc.c, offsets, tiles, num_tiles, ptiles, num_ptiles,
+                 tile_cnt, cnt_len);
   __syncthreads();
   if (f < A) {
     const int pos = s_off[my_e] + s_wh[warp][my_e] + rank_in;
